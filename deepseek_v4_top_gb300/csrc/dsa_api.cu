@@ -1,0 +1,226 @@
+// C ABI of the top-k sparse-attention library: argument checks, launch
+// planning and the small per-device state (error word, decode scratch).
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Decode rows are split into key chunks of this size so that a small batch
+// still spreads over many SMs; each chunk leaves (m, l, O) partials that a
+// second kernel merges in chunk order.  It depends only on the call's shape,
+// so a row's result does not depend on the rest of the batch.
+constexpr int kDecodeChunkKeys = 128;
+
+struct DeviceState {
+    uint32_t* err = nullptr;
+    float* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    int sm_count = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Lazily creates the current device's error word.
+dsa_status device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.err) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED;   // built for sm_103a only
+        uint32_t* e = nullptr;
+        if (cudaMalloc(&e, sizeof(uint32_t)) != cudaSuccess) return DSA_ERR_CUDA;
+        if (cudaMemset(e, 0, sizeof(uint32_t)) != cudaSuccess) {
+            cudaFree(e);
+            return DSA_ERR_CUDA;
+        }
+        st.err = e;
+        st.sm_count = sms;
+    }
+    *out = &st;
+    return DSA_OK;
+}
+
+dsa_status ensure_scratch(DeviceState* st, size_t bytes) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st->scratch_bytes >= bytes) return DSA_OK;
+    if (st->scratch) {
+        // the old buffer may still be read by queued work
+        if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+        cudaFree(st->scratch);
+        st->scratch = nullptr;
+        st->scratch_bytes = 0;
+    }
+    if (cudaMalloc(&st->scratch, bytes) != cudaSuccess) return DSA_ERR_CUDA;
+    st->scratch_bytes = bytes;
+    return DSA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
+                      const float* sink, const float* out, int R, int H, int N, int k_max,
+                      dsa_dtype dtype) {
+    if (R < 0 || N <= 0 || k_max <= 0 || H <= 0) return DSA_ERR_INVALID_ARG;
+    if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    if (H != 16 && H != 32 && H != 64) return DSA_ERR_UNSUPPORTED;
+    if (R == 0) return DSA_OK;
+    if (!q || !kv || !idx || !n_sel || !sink || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+    // 32-bit unit counts and grid limits
+    if (static_cast<long long>(R) * ((k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys) > (1LL << 30))
+        return DSA_ERR_INVALID_ARG;
+    if (dtype == DSA_F32 && R > 65535) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
+               const float* sink, float scale, float* out, int R, int H, int N, int k_max,
+               dsa_dtype dtype, void* stream, bool decode) {
+    dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype);
+    if (st != DSA_OK || R == 0) return st;
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != DSA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (dtype == DSA_F32) {
+        SimtParams p;
+        p.q = static_cast<const float*>(q);
+        p.kv = static_cast<const float*>(kv);
+        p.idx = idx;
+        p.n_sel = n_sel;
+        p.sink = sink;
+        p.out = out;
+        p.err = ds->err;
+        p.scale = scale;
+        p.R = R;
+        p.H = H;
+        p.N = N;
+        p.k_max = k_max;
+        p.decode = decode ? 1 : 0;
+        return launch_simt(p, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    }
+
+    TcParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.kv = static_cast<const uint16_t*>(kv);
+    p.idx = idx;
+    p.n_sel = n_sel;
+    p.sink = sink;
+    p.out = out;
+    p.part = nullptr;
+    p.err = ds->err;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.R = R;
+    p.H = H;
+    p.N = N;
+    p.k_max = k_max;
+    p.decode = decode ? 1 : 0;
+    const int chunks = decode ? (k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys : 1;
+    p.chunk_keys = chunks > 1 ? kDecodeChunkKeys : k_max;
+    p.chunks = chunks;
+    p.units = R * chunks;
+    p.partial = chunks > 1 ? 1 : 0;
+    if (p.partial) {
+        const size_t bytes =
+            static_cast<size_t>(p.units) * (kHeadsPad * kD + 2 * kHeadsPad) * sizeof(float);
+        st = ensure_scratch(ds, bytes);
+        if (st != DSA_OK) return st;
+        p.part = ds->scratch;
+    }
+    const int grid = p.units < ds->sm_count ? p.units : ds->sm_count;
+    if (launch_tc(p, grid, s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (p.partial) {
+        CombineParams c;
+        c.part = p.part;
+        c.sink = sink;
+        c.out = out;
+        c.R = R;
+        c.H = H;
+        c.chunks = chunks;
+        c.units = p.units;
+        if (launch_combine(c, s) != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+dsa_status dsa_sparse_attn_decode(const void* q, const void* kv_cache, const int32_t* idx,
+                                  const int32_t* n_sel, const float* sink, float scale, float* out,
+                                  int B, int H, int N, int k_max, dsa_dtype dtype, void* stream) {
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, B, H, N, k_max, dtype, stream, true);
+}
+
+dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache, const int32_t* idx,
+                                   const int32_t* n_sel, const float* sink, float scale, float* out,
+                                   int R, int H, int N, int k_max, dsa_dtype dtype, void* stream) {
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, false);
+}
+
+dsa_status dsa_get_device_error(void* stream, uint32_t* code) {
+    if (!code) return DSA_ERR_INVALID_ARG;
+    dsa::DeviceState* ds = nullptr;
+    dsa_status st = dsa::device_state(&ds);
+    if (st != DSA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, ds->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaMemset(ds->err, 0, sizeof v) != cudaSuccess) return DSA_ERR_CUDA;
+    *code = v;
+    return DSA_OK;
+}
+
+const char* dsa_status_string(dsa_status status) {
+    switch (status) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+        case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+    }
+    return "DSA_UNKNOWN_STATUS";
+}
+
+dsa_status dsa_shutdown(void) {
+    std::lock_guard<std::mutex> lock(dsa::g_mu);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    dsa_status st = DSA_OK;
+    for (int d = 0; d < dsa::kMaxDevices; ++d) {
+        dsa::DeviceState& ds = dsa::g_dev[d];
+        if (!ds.err && !ds.scratch) continue;
+        if (cudaSetDevice(d) != cudaSuccess) {
+            st = DSA_ERR_CUDA;
+            continue;
+        }
+        if (ds.err) cudaFree(ds.err);
+        if (ds.scratch) cudaFree(ds.scratch);
+        ds = dsa::DeviceState();
+    }
+    if (have_cur) cudaSetDevice(cur);
+    return st;
+}
+
+}  // extern "C"

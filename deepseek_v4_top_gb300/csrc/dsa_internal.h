@@ -1,0 +1,60 @@
+// Internal interface between the host API (dsa_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+constexpr int kD = 512;             // latent row width
+constexpr int kTileKeys = 128;      // keys per tensor-core tile (MMA M)
+constexpr int kHeadsPad = 64;       // heads per tensor-core tile (MMA N)
+
+// One launch of the tensor-core kernel.  A unit is (row, key chunk): keys
+// [chunk * chunk_keys, min((chunk + 1) * chunk_keys, n_sel)) of one row.
+struct TcParams {
+    const uint16_t* q;        // [R][H][512] bf16
+    const uint16_t* kv;       // [N][512] or [R][N][512] bf16
+    const int32_t* idx;       // [R][k_max]
+    const int32_t* n_sel;     // [R]
+    const float* sink;        // [H]
+    float* out;               // final mode: [R][H][512]
+    float* part;              // partial mode: O [units][64][512] then (m, l) [units][2][64]
+    uint32_t* err;            // device error word
+    float scale_log2;         // scale * log2(e)
+    int R, H, N, k_max;
+    int decode;               // 1: row r reads slot r
+    int chunk_keys;           // keys per unit (multiple of 16)
+    int chunks;               // units per row
+    int units;                // R * chunks
+    int partial;              // 1: write partials instead of final outputs
+};
+
+struct SimtParams {
+    const float* q;
+    const float* kv;
+    const int32_t* idx;
+    const int32_t* n_sel;
+    const float* sink;
+    float* out;
+    uint32_t* err;
+    float scale;
+    int R, H, N, k_max;
+    int decode;
+};
+
+struct CombineParams {
+    const float* part;        // as TcParams::part
+    const float* sink;
+    float* out;
+    int R, H, chunks, units;
+};
+
+// Shared memory of the tensor-core kernel (bytes, dynamic).
+size_t tc_smem_bytes();
+
+cudaError_t launch_tc(const TcParams& p, int grid, cudaStream_t s);
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+}  // namespace dsa

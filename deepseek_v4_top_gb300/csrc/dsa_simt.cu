@@ -1,0 +1,174 @@
+// fp32 top-k sparse attention on CUDA cores, and the combine step that merges
+// the per-chunk partial results of a split decode row.
+//
+// fp32 inputs need fp32 products to hold a 1e-5 relative error, which the
+// tf32 tensor-core path cannot give, so this kernel uses FFMA.  One CTA per
+// (head, row); 16-key tiles of gathered rows in shared memory; an exact
+// running maximum per tile (akol1 TensorFold PR #4, first commit message:
+// running maximum, tile sum, value sum), precise expf, the sink folded in at
+// the end (TensorFold PR #1206, "What changes").
+#include <math.h>
+#include <stdint.h>
+
+#include "dsa_internal.h"
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kSimtThreads = 128;
+constexpr int kSimtTile = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+#define DSA_R8(x) x, x, x, x, x, x, x, x
+#define DSA_R64(x) DSA_R8(DSA_R8(x))
+// Source row for an out-of-range selection: NaN everywhere.
+__device__ __align__(16) uint32_t kNanRowF32[512] = {
+    DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u),
+    DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u)};
+
+__global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams p) {
+    __shared__ __align__(16) float qs[kD];
+    __shared__ __align__(16) float kvs[kSimtTile][kD];
+    __shared__ float sc[kSimtTile];
+    __shared__ float ps[kSimtTile];
+
+    const int h = blockIdx.x, r = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const float* qrow = p.q + (static_cast<size_t>(r) * p.H + h) * kD;
+    reinterpret_cast<float4*>(qs)[tid] = reinterpret_cast<const float4*>(qrow)[tid];
+
+    const int ns = p.n_sel[r];
+    const bool bad_n = ns < 0 || ns > p.k_max;
+    if (bad_n && h == 0 && tid == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
+    const int eff = bad_n ? 1 : ns;
+    const float* cache = p.kv + (p.decode ? static_cast<size_t>(r) * p.N * kD : 0);
+    const float* nan_row = reinterpret_cast<const float*>(kNanRowF32);
+
+    float m = -INFINITY, l = 0.0f;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+    for (int t0 = 0; t0 < eff; t0 += kSimtTile) {
+        const int nk = min(kSimtTile, eff - t0);
+        // gather: nk rows, thread tid copies float4 number tid of each row
+        for (int j = 0; j < nk; ++j) {
+            const float* src = nan_row;
+            if (!bad_n) {
+                const int id = p.idx[static_cast<size_t>(r) * p.k_max + t0 + j];
+                if (id >= 0 && id < p.N) {
+                    src = cache + static_cast<size_t>(id) * kD;
+                } else if (h == 0 && tid == 0) {
+                    atomicOr(p.err, DSA_DEVERR_IDX_RANGE);
+                }
+            }
+            reinterpret_cast<float4*>(kvs[j])[tid] = reinterpret_cast<const float4*>(src)[tid];
+        }
+        __syncthreads();
+        // scores: warp w takes keys 4w .. 4w+3; lane sums d = lane + 32 i in order
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = warp * 4 + jj;
+            if (j < nk) {
+                float part = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kD / 32; ++i) part = fmaf(qs[lane + 32 * i], kvs[j][lane + 32 * i], part);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) sc[j] = part * p.scale;
+            }
+        }
+        __syncthreads();
+        float tm = -INFINITY;
+        for (int j = 0; j < nk; ++j) tm = fmaxf(tm, sc[j]);
+        const float mn = (m == -INFINITY) ? tm : fmaxf(m, tm);
+        const float mu_new = (mn == -INFINITY) ? 0.0f : mn;
+        const float al = (m == -INFINITY) ? 1.0f : expf(m - mu_new);
+        if (tid < nk) ps[tid] = expf(sc[tid] - mu_new);
+        __syncthreads();
+        float ls = 0.0f;
+        for (int j = 0; j < nk; ++j) ls += ps[j];
+        l = l * al + ls;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d = tid + 128 * i;
+            float a = acc[i] * al;
+            for (int j = 0; j < nk; ++j) a = fmaf(ps[j], kvs[j][d], a);
+            acc[i] = a;
+        }
+        m = mn;
+        __syncthreads();
+    }
+
+    // sink fold: out = acc * e^{mu - m*} / (l e^{mu - m*} + e^{sink - m*})
+    const float mu = (m == -INFINITY) ? 0.0f : m;
+    const float sk = p.sink[h];
+    const float mstar = isfinite(sk) ? fmaxf(mu, sk) : mu;
+    const float e1 = expf(mu - mstar);
+    const float e2 = expf(sk - mstar);
+    const float f = e1 / (l * e1 + e2);
+    float* orow = p.out + (static_cast<size_t>(r) * p.H + h) * kD;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = acc[i] * f;
+}
+
+// One CTA per (row, group of 8 heads); thread t owns columns 4t .. 4t+3.
+// Partials of one row are merged in chunk order, so the result is
+// deterministic.  Each partial holds (m, l, O) with O and l relative to
+// 2^m (2^0 when m is -inf, in which case O and l are 0 or NaN).
+__global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p) {
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
+    for (int hh = 0; hh < 8; ++hh) {
+        const int h = blockIdx.y * 8 + hh;
+        if (h >= p.H) break;
+        float M = -INFINITY;
+        bool have = false;
+        for (int c = 0; c < p.chunks; ++c) {
+            const float mc = ml_base[(static_cast<size_t>(r) * p.chunks + c) * 2 * kHeadsPad + h];
+            if (mc != -INFINITY) {
+                M = have ? fmaxf(M, mc) : mc;
+                have = true;
+            }
+        }
+        const float mu = have ? M : 0.0f;
+        float l = 0.0f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < p.chunks; ++c) {
+            const size_t u = static_cast<size_t>(r) * p.chunks + c;
+            const float mc = ml_base[u * 2 * kHeadsPad + h];
+            const float lc = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
+            const float w = (mc == -INFINITY) ? 1.0f : exp2f(mc - mu);
+            l += w * lc;
+            const float4 o = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+        const float s2 = p.sink[h] * kLog2e;
+        const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
+        const float e1 = exp2f(mu - mstar);
+        const float e2 = exp2f(s2 - mstar);
+        const float f = e1 / (l * e1 + e2);
+        float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+        reinterpret_cast<float4*>(p.out + (static_cast<size_t>(r) * p.H + h) * kD)[tid] = res;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t s) {
+    dim3 grid(p.H, p.R);
+    dsa_simt_kernel<<<grid, kSimtThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
+    dim3 grid(p.R, (p.H + 7) / 8);
+    dsa_combine_kernel<<<grid, 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,166 @@
+"""Python binding of libdsa.so: the C ABI of include/dsa.h under the same names.
+
+Argument marshalling only.  Every step of the attention runs in the CUDA
+kernels of libdsa.so; PyTorch provides device memory and the current stream.
+There is no fallback: if the library is missing or the GPU is unsupported,
+the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdsa.so")
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARG = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_CUDA = 3
+DSA_ERR_DEVICE_CHECK = 4
+
+DSA_F32 = 0
+DSA_BF16 = 1
+
+DSA_DEVERR_IDX_RANGE = 0x1
+DSA_DEVERR_NSEL_RANGE = 0x2
+DSA_DEVERR_TIMEOUT = 0x4
+DSA_DEVERR_LAYOUT = 0x8
+
+# Every function declared in include/dsa.h.
+EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_get_device_error",
+           "dsa_status_string", "dsa_shutdown")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s returned %s" % (where, status_string(status)))
+
+
+def load():
+    """Load libdsa.so (it must have been built; see __graft_entry__.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libdsa.so is not built: run __graft_entry__.build() first")
+            lib = ctypes.CDLL(LIB_PATH)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            sig = [P, P, P, P, P, F, P, I, I, I, I, I, P]
+            for name in ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill"):
+                fn = getattr(lib, name)
+                fn.argtypes = sig
+                fn.restype = I
+            lib.dsa_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            lib.dsa_get_device_error.restype = I
+            lib.dsa_status_string.argtypes = [I]
+            lib.dsa_status_string.restype = ctypes.c_char_p
+            lib.dsa_shutdown.argtypes = []
+            lib.dsa_shutdown.restype = I
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().dsa_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------- raw pointers
+def call_raw(name: str, q: int, kv: int, idx: int, n_sel: int, sink: int, scale: float, out: int,
+             R: int, H: int, N: int, k_max: int, dtype: int, stream: int = 0) -> int:
+    """Call an entry point with integer device addresses; returns the status."""
+    fn = getattr(load(), name)
+    return int(fn(q, kv, idx, n_sel, sink, ctypes.c_float(scale), out, R, H, N, k_max, dtype,
+                  stream))
+
+
+# ------------------------------------------------------------ torch tensors
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return DSA_F32
+    if t.dtype == torch.bfloat16:
+        return DSA_BF16
+    raise TypeError("q and kv_cache must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _check(q, kv, idx, n_sel, sink, out, decode):
+    import torch
+    for name, t in (("q", q), ("kv_cache", kv), ("idx", idx), ("n_sel", n_sel), ("sink", sink),
+                    ("out", out)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if kv.dtype != q.dtype:
+        raise TypeError("q and kv_cache must have the same dtype")
+    if idx.dtype != torch.int32 or n_sel.dtype != torch.int32:
+        raise TypeError("idx and n_sel must be int32")
+    if sink.dtype != torch.float32 or out.dtype != torch.float32:
+        raise TypeError("sink and out must be float32")
+    if q.dim() != 3 or q.shape[2] != 512:
+        raise ValueError("q must be [rows, heads, 512]")
+    R, H = q.shape[0], q.shape[1]
+    if decode:
+        if kv.dim() != 3 or kv.shape[0] != R or kv.shape[2] != 512:
+            raise ValueError("decode kv_cache must be [B, N, 512]")
+        N = kv.shape[1]
+    else:
+        if kv.dim() != 2 or kv.shape[1] != 512:
+            raise ValueError("prefill kv_cache must be [N, 512]")
+        N = kv.shape[0]
+    if idx.dim() != 2 or idx.shape[0] != R:
+        raise ValueError("idx must be [rows, k_max]")
+    if tuple(n_sel.shape) != (R,) or tuple(sink.shape) != (H,) or tuple(out.shape) != (R, H, 512):
+        raise ValueError("n_sel [rows], sink [heads] and out [rows, heads, 512] expected")
+    return R, H, N, idx.shape[1]
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _run(name, decode, q, kv_cache, idx, n_sel, sink, scale, out, stream):
+    R, H, N, k_max = _check(q, kv_cache, idx, n_sel, sink, out, decode)
+    st = call_raw(name, q.data_ptr(), kv_cache.data_ptr(), idx.data_ptr(), n_sel.data_ptr(),
+                  sink.data_ptr(), float(scale), out.data_ptr(), R, H, N, k_max,
+                  _dtype_code(q), _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, name)
+    return out
+
+
+def dsa_sparse_attn_decode(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
+    """Decode attention: q [B,H,512], kv_cache [B,N,512], out [B,H,512] fp32."""
+    return _run("dsa_sparse_attn_decode", True, q, kv_cache, idx, n_sel, sink, scale, out, stream)
+
+
+def dsa_sparse_attn_prefill(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
+    """Prefill attention: q [R,H,512], kv_cache [N,512], out [R,H,512] fp32."""
+    return _run("dsa_sparse_attn_prefill", False, q, kv_cache, idx, n_sel, sink, scale, out, stream)
+
+
+def dsa_get_device_error(stream=None) -> int:
+    """Synchronise the stream, return and clear the device error word."""
+    code = ctypes.c_uint32(0)
+    st = load().dsa_get_device_error(_stream_handle(stream), ctypes.byref(code))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_get_device_error")
+    return int(code.value)
+
+
+def dsa_shutdown() -> None:
+    st = load().dsa_shutdown()
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_shutdown")

@@ -1,0 +1,133 @@
+/*
+ * dsa.h -- C ABI of a GB300 (sm_103a) library for DeepSeek-V4.1 top-k sparse
+ * attention.
+ *
+ * The operation (akol1 TensorFold PR #4, first commit message; TensorFold
+ * PR #1206, "What changes"): for each query row r and head h, gather the
+ * n_sel[r] latent KV rows x_j = kv[slot(r)][idx[r][j]] that an indexer
+ * selected, score them, and return the softmax-weighted sum of the same rows
+ * with one extra per-head sink logit in the denominator:
+ *
+ *   s_j = scale * <q[r][h][:], x_j>          (the 512-wide row is key and value)
+ *   out[r][h][:] = sum_j e^{s_j} x_j / (e^{sink[h]} + sum_j e^{s_j})
+ *
+ * computed tile by tile with a running maximum, a running sum and a running
+ * value sum.  The sink is a logit (it is not multiplied by scale) and has no
+ * value row.  The latent row is 512 wide, handled as sixteen 32-wide column
+ * groups on the pages; here it is one contiguous row.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array arguments are DEVICE pointers owned by the caller.  The
+ *   library never frees or retains them.  Row-major, contiguous:
+ *     q     [R][H][512]    dtype (float32, or bfloat16 bit patterns)
+ *     kv    prefill: [N][512] (one cache shared by all rows)
+ *           decode:  [B][N][512] (row b reads only slot b)
+ *     idx   [R][k_max] int32; only the first n_sel[r] entries are read
+ *     n_sel [R] int32
+ *     sink  [H] float32 (any value, including +-inf)
+ *     out   [R][H][512] float32; must not overlap any input
+ *   q, kv and out must be 16-byte aligned.
+ * - H must be 16, 32 or 64; the row width is fixed at 512.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream) and run on the current device.  The library allocates
+ *   nothing per call: a 4-byte device error word and, for decode, one scratch
+ *   buffer for split partial results are allocated once per device on first
+ *   use (the scratch grows when a larger batch needs it) and released by
+ *   dsa_shutdown().  Do not issue the first call of a device inside a CUDA
+ *   graph capture.
+ * - Host-side errors return before anything is launched.
+ * - Device-side errors: an index in idx[r][0..n_sel[r]) outside [0, N), or an
+ *   n_sel[r] outside [0, k_max], sets a bit in a sticky device error word and
+ *   writes NaN to every output of that row; the kernels never trap.  Read
+ *   (and clear) the word with dsa_get_device_error().
+ * - Numerics: float32 inputs run on CUDA cores in fp32 with precise expf; bf16
+ *   inputs run on the tensor cores (bf16 products, fp32 accumulation, the
+ *   softmax weights split into two bf16 terms), fp32 softmax.  Results are
+ *   bit-identical from run to run and do not depend on the other rows of the
+ *   batch.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad alignment        */
+    DSA_ERR_UNSUPPORTED = 2,   /* H not in {16,32,64}, unknown dtype, no GPU   */
+    DSA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
+    DSA_ERR_DEVICE_CHECK = 4   /* reserved: returned by no call at present     */
+} dsa_status;
+
+typedef enum {
+    DSA_F32 = 0,               /* q and kv are float32                         */
+    DSA_BF16 = 1               /* q and kv are bfloat16                        */
+} dsa_dtype;
+
+/* Bits of the device error word. */
+#define DSA_DEVERR_IDX_RANGE  0x1u  /* an idx entry outside [0, N)                */
+#define DSA_DEVERR_NSEL_RANGE 0x2u  /* an n_sel entry outside [0, k_max]          */
+#define DSA_DEVERR_TIMEOUT    0x4u  /* a bounded in-kernel wait gave up; the
+                                       outputs of that launch are undefined      */
+#define DSA_DEVERR_LAYOUT     0x8u  /* shared memory not 1024-byte aligned; the
+                                       kernel did no work                        */
+
+/*
+ * Decode: B slots with one query row each.  Row b attends to k <= k_max
+ * positions of its own cache kv[b] (N positions).  On the pages this is a
+ * decode step's attention call (akol1 TensorFold PR #4; "warm attention call"
+ * timings at positions 128 and 8191).
+ *   q [B][H][512], kv [B][N][512], idx [B][k_max], n_sel [B], out [B][H][512].
+ * Returns DSA_OK after queueing the work (B == 0 queues nothing).
+ */
+DSA_API dsa_status dsa_sparse_attn_decode(const void* q, const void* kv_cache,
+                                          const int32_t* idx, const int32_t* n_sel,
+                                          const float* sink, float scale, float* out,
+                                          int B, int H, int N, int k_max,
+                                          dsa_dtype dtype, void* stream);
+
+/*
+ * Prefill: R query rows of one segment attend to one shared cache of N
+ * positions (TensorFold PR #1206: 2048-row prefill segments; a row at
+ * position p selects min(p+1, k) positions in [0, p]).
+ *   q [R][H][512], kv [N][512], idx [R][k_max], n_sel [R], out [R][H][512].
+ * Returns DSA_OK after queueing the work (R == 0 queues nothing).
+ */
+DSA_API dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache,
+                                           const int32_t* idx, const int32_t* n_sel,
+                                           const float* sink, float scale, float* out,
+                                           int R, int H, int N, int k_max,
+                                           dsa_dtype dtype, void* stream);
+
+/*
+ * Synchronises `stream`, stores the current device's error word in *code
+ * and clears it.  *code is 0 when no launch since the last read found a
+ * problem.  DSA_ERR_INVALID_ARG if code is NULL; DSA_ERR_CUDA if the
+ * synchronisation or the copy fails.
+ */
+DSA_API dsa_status dsa_get_device_error(void* stream, uint32_t* code);
+
+/* Static, human-readable name of a status code. */
+DSA_API const char* dsa_status_string(dsa_status status);
+
+/*
+ * Releases the per-device error word and scratch of every device the
+ * library touched.  Call only when no launch of this library is pending.
+ */
+DSA_API dsa_status dsa_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

@@ -1,0 +1,88 @@
+"""The C-ABI library: it loads, exports every declared symbol, and rejects
+bad host-side arguments before touching the GPU (CPU only)."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from deepseek_v4_top_gb300 import dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deepseek_v4_top_gb300 import build
+    build.build()
+    return dsa.load()
+
+
+def _declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:DSA_API\s+)?(?:const\s+)?\w+[\s\*]+(dsa_\w+)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "dsa_sparse_attn_decode" in names and "dsa_sparse_attn_prefill" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(dsa.EXPORTS)
+
+
+def test_only_the_c_abi_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", dsa.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {n for n in exported if n.startswith("dsa")}
+    assert ours == set(dsa.EXPORTS)
+
+
+def test_status_strings(lib):
+    assert dsa.status_string(0) == "DSA_OK"
+    assert dsa.status_string(1) == "DSA_ERR_INVALID_ARG"
+    assert dsa.status_string(2) == "DSA_ERR_UNSUPPORTED"
+    assert dsa.status_string(3) == "DSA_ERR_CUDA"
+    assert dsa.status_string(4) == "DSA_ERR_DEVICE_CHECK"
+    assert dsa.status_string(99) == "DSA_UNKNOWN_STATUS"
+
+
+FAKE = 1 << 20     # a 16-byte-aligned non-null address; never dereferenced
+
+
+@pytest.mark.parametrize("name", ["dsa_sparse_attn_decode", "dsa_sparse_attn_prefill"])
+def test_host_validation_before_any_launch(lib, name):
+    good = dict(q=FAKE, kv=FAKE, idx=FAKE, n_sel=FAKE, sink=FAKE, scale=0.1, out=FAKE,
+                R=2, H=64, N=100, k_max=8, dtype=dsa.DSA_BF16)
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        return dsa.call_raw(name, a["q"], a["kv"], a["idx"], a["n_sel"], a["sink"], a["scale"],
+                            a["out"], a["R"], a["H"], a["N"], a["k_max"], a["dtype"])
+
+    for ptr in ("q", "kv", "idx", "n_sel", "sink", "out"):
+        assert call(**{ptr: 0}) == dsa.DSA_ERR_INVALID_ARG
+    assert call(q=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG        # misaligned
+    assert call(out=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
+    assert call(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert call(N=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(k_max=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(H=0) == dsa.DSA_ERR_INVALID_ARG
+    for h in (8, 48, 128):
+        assert call(H=h) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(dtype=7) == dsa.DSA_ERR_UNSUPPORTED
+    # nothing to do: returns before any device work
+    assert call(R=0, q=0, out=0) == dsa.DSA_OK
+
+
+def test_device_error_query_rejects_null(lib):
+    assert lib.dsa_get_device_error(None, None) == dsa.DSA_ERR_INVALID_ARG
