@@ -1,0 +1,457 @@
+"""Benchmark of the top-k sparse-attention hot path on GB300.
+
+One step = one batched decode call (8 slots x 32768-position caches) and one
+prefill call (2048 rows at positions 2048..4095 of a 4096-position cache), both
+with 64 heads, 512-wide latent rows, k = 640 selected keys, bf16 inputs.
+Metric: row*heads per second (whole job), plus gathered-KV GB/s per workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same per-GPU workload (weak scaling); the
+step time is the maximum over ranks.  --impl reference times the fp64 CPU
+oracle on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deepseek_v4_top_gb300 import inputs as I  # noqa: E402
+
+H, D, K = 64, 512, 640
+DEC_B, DEC_N = 8, 32768
+PRE_R, PRE_N = 2048, 4096
+METRIC = "sparse-attn row·heads/s and HBM GB/s at H=64,d=512,k=640 (decode B=8, prefill 2048)"
+WORKLOAD = ("decode B=8 x 1 row (N=32768 per slot) + prefill 2048 rows (positions 2048..4095, "
+            "N=4096); H=64, d=512, k=640, bf16 q/kv, fp32 out")
+UNITS_PER_STEP = (DEC_B + PRE_R) * H        # row*heads
+FLOPS_PER_ROW = 4 * H * D * K              # q.k and p.v, one row, all heads
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "of measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "of fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Maximum of a per-rank float over the process group (identity when alone)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 + 0.05] or [s for (_, s) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if len(r) > 1 and num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if len(r) > 2 and num(r[2]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- traffic
+def recorded_traffic():
+    """DRAM bytes per prefill launch from the committed ncu summary, if the
+    kernel source is still the one the counters were taken on."""
+    path = os.path.join(ROOT, "profiles", "dsa_tc_kernel_prefill2048.md")
+    src = os.path.join(ROOT, "deepseek_v4_top_gb300", "csrc", "dsa_tc.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.e+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(pre, dec, target_s: float, rows_cap: int = PRE_R):
+    """Time the fp64 oracle on whole rows (all 64 heads) of both workloads,
+    growing the sample until it takes about target_s.  Returns
+    (row_heads_per_s, threads, description)."""
+    import oracle
+    oracle.build()
+    def timed(n_pre, n_dec):
+        t0 = time.perf_counter()
+        used = 1
+        if n_pre:
+            rows = np.repeat(np.arange(n_pre, dtype=np.int32), H)
+            heads = np.tile(np.arange(H, dtype=np.int32), n_pre)
+            _, used = oracle.pairs(pre, rows, heads)
+        if n_dec:
+            rows = np.repeat(np.arange(n_dec, dtype=np.int32), H)
+            heads = np.tile(np.arange(H, dtype=np.int32), n_dec)
+            _, used = oracle.pairs(dec, rows, heads)
+        return time.perf_counter() - t0, used
+    dt, used = timed(1, 1)
+    n = max(1, min(rows_cap, int(target_s / max(dt, 1e-6))))
+    n_dec = min(n, dec.R)
+    dt, used = timed(n, n_dec)
+    units = (n + n_dec) * H
+    desc = ("%d prefill rows + %d decode rows x 64 heads (k=640 each), fp64 oracle, %d threads"
+            % (n, n_dec, used))
+    return units / dt, used, desc
+
+
+# ------------------------------------------------------------------ ours
+def bench_ours(args, world, rank, local):
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    do_dec = args.workload in ("both", "decode")
+    do_pre = args.workload in ("both", "prefill")
+
+    dec = I.batched_decode(B=DEC_B, N=DEC_N) if do_dec else None
+    pre = I.prefill(rows=PRE_R, N=PRE_N) if do_pre else None
+
+    def up(a, bf16):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else a)
+        return t.to(dev).view(torch.bfloat16) if bf16 else t.to(dev)
+
+    def upload(c):
+        return dict(q=up(c.q, True), kv=up(c.kv, True), idx=up(c.idx, False),
+                    n_sel=up(c.n_sel, False), sink=up(c.sink, False))
+
+    d_dec = upload(dec) if do_dec else None
+    d_pre = upload(pre) if do_pre else None
+    o_dec = torch.empty((DEC_B, H, D), dtype=torch.float32, device=dev) if do_dec else None
+    o_pre = torch.empty((PRE_R, H, D), dtype=torch.float32, device=dev) if do_pre else None
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call_dec():
+        if do_dec:
+            dsa.dsa_sparse_attn_decode(d_dec["q"], d_dec["kv"], d_dec["idx"], d_dec["n_sel"],
+                                       d_dec["sink"], dec.scale, o_dec, stream)
+
+    def call_pre():
+        if do_pre:
+            dsa.dsa_sparse_attn_prefill(d_pre["q"], d_pre["kv"], d_pre["idx"], d_pre["n_sel"],
+                                        d_pre["sink"], pre.scale, o_pre, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call_dec()
+        call_pre()
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(float(i))            # evict L2 between steps (outside the events)
+        ev[i][0].record(stream)
+        call_dec()
+        ev[i][1].record(stream)
+        call_pre()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    pre_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    dec_avg = reduce_max(sum(dec_ms) / args.steps, world)
+    pre_avg = reduce_max(sum(pre_ms) / args.steps, world)
+    step_ms = reduce_max(sum(dec_ms) / args.steps + sum(pre_ms) / args.steps, world)
+    assert dsa.dsa_get_device_error() == 0
+
+    # end to end through the public API: host (pinned) inputs in, result out
+    pinned = []
+
+    def pin(a):
+        t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        pinned.append(t)
+        return t
+
+    e2e_io = []
+    if do_dec:
+        e2e_io.append((d_dec, pin(dec.q.view(np.int16)), pin(dec.idx), pin(dec.n_sel),
+                       torch.empty(o_dec.shape, dtype=torch.float32).pin_memory(), o_dec, call_dec))
+    if do_pre:
+        e2e_io.append((d_pre, pin(pre.q.view(np.int16)), pin(pre.idx), pin(pre.n_sel),
+                       torch.empty(o_pre.shape, dtype=torch.float32).pin_memory(), o_pre, call_pre))
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = sum(io[4].numel() * 4 for io in e2e_io)
+
+    def e2e_step():
+        for d, hq, hidx, hns, hout, dout, call in e2e_io:
+            d["q"].view(torch.int16).copy_(hq, non_blocking=True)
+            d["idx"].copy_(hidx, non_blocking=True)
+            d["n_sel"].copy_(hns, non_blocking=True)
+            call()
+            hout.copy_(dout, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world)
+    t_clock1 = time.time()
+    clocks.stop()
+    assert dsa.dsa_get_device_error() == 0
+    for o in (o_dec, o_pre):
+        if o is not None:
+            assert torch.isfinite(o).all().item()
+
+    pk, pk_note = peaks()
+    units = ((DEC_B if do_dec else 0) + (PRE_R if do_pre else 0)) * H
+    value = units * world / (step_ms * 1e-3)
+    workloads = {}
+    if do_dec:
+        g = DEC_B * K * D * 2
+        workloads["decode_b8"] = {
+            "ms": dec_avg, "row_heads_per_s": DEC_B * H / (dec_avg * 1e-3),
+            "gathered_kv_gbs": g / (dec_avg * 1e-3) / 1e9,
+            "gathered_frac_hbm": g / (dec_avg * 1e-3) / 1e9 / pk["hbm_gbs"], "launches": 2}
+    roofline = None
+    if do_pre:
+        g = PRE_R * K * D * 2
+        pre_flops = FLOPS_PER_ROW * PRE_R
+        pre_tflops = pre_flops / (pre_avg * 1e-3) / 1e12
+        workloads["prefill_2048"] = {
+            "ms": pre_avg, "row_heads_per_s": PRE_R * H / (pre_avg * 1e-3),
+            "gathered_kv_gbs": g / (pre_avg * 1e-3) / 1e9,
+            "gathered_frac_hbm": g / (pre_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "tflops": pre_tflops, "launches": 1}
+        roofline = {
+            "kernel": "dsa_tc_kernel (prefill 2048)",
+            "bound": "tensor",
+            "achieved": pre_tflops,
+            "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": pre_tflops / pk["bf16_tflops"],
+            "peak_note": "bf16 burst " + pk_note + " (kernel timed alone)",
+            "algorithmic_per_launch": "4*H*d*k flops per row x 2048 rows = %.4g FLOP" % pre_flops,
+            "traffic": recorded_traffic(),
+        }
+    else:
+        g = DEC_B * K * D * 2
+        a = g / (dec_avg * 1e-3) / 1e9
+        roofline = {"kernel": "dsa_tc_kernel + dsa_combine_kernel (decode B=8)", "bound": "hbm",
+                    "achieved": a, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": a / pk["hbm_gbs"],
+                    "peak_note": "copy bandwidth " + pk_note,
+                    "algorithmic_per_launch": "8 rows x 640 keys x 1024 B gathered", "traffic": None}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "row*heads/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/kv, seeded distinct and causal top-k indices)",
+        "config": {
+            "workload": WORKLOAD if args.workload == "both" else args.workload + " part of: " + WORKLOAD,
+            "decode": {"B": DEC_B, "N": DEC_N}, "prefill": {"rows": PRE_R, "N": PRE_N},
+            "heads": H, "d": D, "k": K,
+            "parallelism": "dp%d (independent replicas, no collective)" % world,
+            "l2": "flushed before every step by writing 2x L2; events bracket the calls only",
+        },
+        "workloads": workloads,
+        "roofline": roofline,
+        "gpu_launches": (2 * do_dec + do_pre) * args.steps,
+        "e2e": {
+            "value": units * world / (e2e_ms * 1e-3),
+            "unit": "row*heads/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "q, idx, n_sel copied in from pinned host memory and out copied back every "
+                    "step; KV caches and sinks stay resident",
+        },
+        "clocks": clocks.summary(t_wall0, t_clock1),
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    if rank == 0 and not args.no_cpu_baseline and do_dec and do_pre:
+        v, cores, desc = oracle_sample(pre, dec, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "row*heads/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- reference
+def bench_reference(args, world, rank):
+    """The fp64 CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dec = I.batched_decode(B=DEC_B, N=DEC_N)
+    pre = I.prefill(rows=PRE_R, N=PRE_N)
+    # each step: one decode row and one prefill row, all 64 heads
+    rows = np.repeat(np.arange(1, dtype=np.int32), H)
+    heads = np.arange(H, dtype=np.int32)
+    threads = 1
+
+    def step(i):
+        nonlocal threads
+        rp = np.full(H, i % PRE_R, np.int32)
+        rd = np.full(H, i % DEC_B, np.int32)
+        _, threads = oracle.pairs(pre, rp, heads)
+        _, threads = oracle.pairs(dec, rd, heads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = (time.perf_counter() - t0) / args.steps
+    units = 2 * H
+    v = units / dt
+    desc = ("per step: 1 prefill row + 1 decode row x 64 heads (k=640), fp64 oracle, %d threads"
+            % threads)
+    del rows
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": v, "unit": "row*heads/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same generator and seeds as the GPU arm)",
+        "config": {"workload": WORKLOAD, "heads": H, "d": D, "k": K,
+                   "parallelism": "host cores of rank 0"},
+        "cpu_baseline": {"value": v, "unit": "row*heads/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": v, "unit": "row*heads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="approximate CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("both", "prefill", "decode"), default="both",
+                    help="both (the benchmark step) or one half of it, for profiling")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+    else:
+        bench_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -79,7 +79,7 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
                       dsa_dtype dtype) {
     if (R < 0 || N <= 0 || k_max <= 0 || H <= 0) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
-    if (H != 16 && H != 32 && H != 64) return DSA_ERR_UNSUPPORTED;
+    if (H > kHeadsPad) return DSA_ERR_UNSUPPORTED;   // heads are padded to 64 on chip
     if (R == 0) return DSA_OK;
     if (!q || !kv || !idx || !n_sel || !sink || !out) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_INVALID_ARG;

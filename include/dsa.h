@@ -28,7 +28,8 @@
  *     sink  [H] float32 (any value, including +-inf)
  *     out   [R][H][512] float32; must not overlap any input
  *   q, kv and out must be 16-byte aligned.
- * - H must be 16, 32 or 64; the row width is fixed at 512.
+ * - 1 <= H <= 64 (the pages use 64 heads, 16 or 32 a rank under tensor
+ *   parallelism); the row width is fixed at 512.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *   default stream) and run on the current device.  The library allocates
  *   nothing per call: a 4-byte device error word and, for decode, one scratch
@@ -65,7 +66,7 @@ extern "C" {
 typedef enum {
     DSA_OK = 0,
     DSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad alignment        */
-    DSA_ERR_UNSUPPORTED = 2,   /* H not in {16,32,64}, unknown dtype, no GPU   */
+    DSA_ERR_UNSUPPORTED = 2,   /* H > 64, unknown dtype, not an sm_103 GPU     */
     DSA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
     DSA_ERR_DEVICE_CHECK = 4   /* reserved: returned by no call at present     */
 } dsa_status;

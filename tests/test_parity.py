@@ -145,13 +145,17 @@ def test_rows_do_not_depend_on_their_batch():
 def test_out_of_range_selection_sets_error_and_nan_row(dtype, mode):
     from deepseek_v4_top_gb300 import dsa
     rng = np.random.default_rng(8)
-    c = I._edge_base(rng, "bad", dtype, 32, 300, mode, R=4, N=1000, k_extra=0)
+    c = I._edge_base(rng, "bad", dtype, 32, 300, mode, R=5, N=1000, k_extra=0)
+    for r in range(c.R):
+        c.idx[r] = rng.choice(c.N, c.k_max, replace=False)
+    c.n_sel[:] = c.k_max
     c.idx[1, 5] = c.N            # index == N
     c.idx[2, 299] = -3           # negative index, in the last partial tile
     c.n_sel[3] = c.k_max + 1     # n_sel beyond k_max
     got, code = run(c)
     assert code == (dsa.DSA_DEVERR_IDX_RANGE | dsa.DSA_DEVERR_NSEL_RANGE)
-    assert np.isnan(got[1:]).all()
+    assert np.isnan(got[1:4]).all()
+    assert np.isfinite(got[0]).all() and np.isfinite(got[4]).all()
     ref, _ = oracle.attn(c)
     compare(c, got, ref)          # the oracle's contract gives the same NaN rows
     assert dsa.dsa_get_device_error() == 0      # reading cleared the word
