@@ -14,11 +14,6 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Decode rows are split into key chunks of this size so that a small batch
-// still spreads over many SMs; each chunk leaves (m, l, O) partials that a
-// second kernel merges in chunk order.  It depends only on the call's shape,
-// so a row's result does not depend on the rest of the batch.
-constexpr int kDecodeChunkKeys = 128;
 
 struct DeviceState {
     uint32_t* err = nullptr;
@@ -140,7 +135,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     p.partial = chunks > 1 ? 1 : 0;
     if (p.partial) {
         const size_t bytes =
-            static_cast<size_t>(p.units) * (kHeadsPad * kD + 2 * kHeadsPad) * sizeof(float);
+            static_cast<size_t>(p.units) * kPartialFloats * sizeof(float);
         st = ensure_scratch(ds, bytes);
         if (st != DSA_OK) return st;
         p.part = ds->scratch;

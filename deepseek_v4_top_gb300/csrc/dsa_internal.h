@@ -9,6 +9,13 @@ namespace dsa {
 constexpr int kD = 512;             // latent row width
 constexpr int kTileKeys = 128;      // keys per tensor-core tile (MMA M)
 constexpr int kHeadsPad = 64;       // heads per tensor-core tile (MMA N)
+// Decode rows are split into key chunks of this size so that a small batch
+// still spreads over many SMs; each chunk leaves (m, l, O) partials that a
+// second kernel merges in chunk order.  It depends only on the call's shape,
+// so a row's result does not depend on the rest of the batch.
+constexpr int kDecodeChunkKeys = 128;
+// Floats of one chunk's partial result: O [64][512] plus (m, l) [2][64].
+constexpr size_t kPartialFloats = static_cast<size_t>(kHeadsPad) * kD + 2 * kHeadsPad;
 
 // One launch of the tensor-core kernel.  A unit is (row, key chunk): keys
 // [chunk * chunk_keys, min((chunk + 1) * chunk_keys, n_sel)) of one row.

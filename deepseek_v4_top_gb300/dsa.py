@@ -30,8 +30,9 @@ DSA_DEVERR_TIMEOUT = 0x4
 DSA_DEVERR_LAYOUT = 0x8
 
 # Every function declared in include/dsa.h.
-EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_get_device_error",
-           "dsa_status_string", "dsa_shutdown")
+EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_sparse_attn_decode_noalloc",
+           "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
+DSA_NOALLOC_MAX_UNITS = 64
 
 _lib = None
 _lock = threading.Lock()
@@ -53,7 +54,8 @@ def load():
             lib = ctypes.CDLL(LIB_PATH)
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             sig = [P, P, P, P, P, F, P, I, I, I, I, I, P]
-            for name in ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill"):
+            for name in ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
+                         "dsa_sparse_attn_decode_noalloc"):
                 fn = getattr(lib, name)
                 fn.argtypes = sig
                 fn.restype = I
@@ -149,6 +151,13 @@ def dsa_sparse_attn_decode(q, kv_cache, idx, n_sel, sink, scale, out, stream=Non
 def dsa_sparse_attn_prefill(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
     """Prefill attention: q [R,H,512], kv_cache [N,512], out [R,H,512] fp32."""
     return _run("dsa_sparse_attn_prefill", False, q, kv_cache, idx, n_sel, sink, scale, out, stream)
+
+
+def dsa_sparse_attn_decode_noalloc(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
+    """Decode attention that allocates no device memory (fixed static scratch;
+    see include/dsa.h for its size limit and its sharing rules)."""
+    return _run("dsa_sparse_attn_decode_noalloc", True, q, kv_cache, idx, n_sel, sink, scale, out,
+                stream)
 
 
 def dsa_get_device_error(stream=None) -> int:

@@ -112,6 +112,43 @@ DSA_API dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache,
                                            dsa_dtype dtype, void* stream);
 
 /*
+ * Largest number of (row, 128-key chunk) units that
+ * dsa_sparse_attn_decode_noalloc() accepts: B * ceil(k_max / 128) <= 64,
+ * e.g. 8 rows with k_max <= 1024.
+ */
+#define DSA_NOALLOC_MAX_UNITS 64
+
+/*
+ * Decode without any device allocation.  The pages have no counterpart to
+ * this entry point; it exists for callers of this library that must not
+ * allocate device memory: engines that reserve all device memory when they
+ * start and forbid allocation afterwards, and callers on a latency-critical
+ * path where cudaMalloc / cudaFree would synchronise the device.
+ *
+ * Same arguments, layouts and results as dsa_sparse_attn_decode() (the same
+ * kernels with the same key chunking), bf16 only.  The split partials and an
+ * error word live in one static device array of 8,421,632 bytes, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing; the caller still passes all inputs and outputs.
+ *
+ * - Returns DSA_ERR_UNSUPPORTED when B * ceil(k_max / 128) exceeds
+ *   DSA_NOALLOC_MAX_UNITS, or for float32 inputs; DSA_ERR_INVALID_ARG for the
+ *   same bad arguments as dsa_sparse_attn_decode().
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ * - Every call uses the same array and it keeps the last call's contents:
+ *   calls whose work overlaps on the GPU (other streams, other threads) race
+ *   and corrupt each other's results.  Order them on one stream.
+ * - Out-of-range selections still give NaN rows, but their error bits are not
+ *   reported through dsa_get_device_error().
+ */
+DSA_API dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_cache,
+                                                  const int32_t* idx, const int32_t* n_sel,
+                                                  const float* sink, float scale, float* out,
+                                                  int B, int H, int N, int k_max,
+                                                  dsa_dtype dtype, void* stream);
+
+/*
  * Synchronises `stream`, stores the current device's error word in *code
  * and clears it.  *code is 0 when no launch since the last read found a
  * problem.  DSA_ERR_INVALID_ARG if code is NULL; DSA_ERR_CUDA if the
