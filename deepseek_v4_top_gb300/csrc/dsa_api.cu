@@ -82,6 +82,9 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
     if (static_cast<long long>(R) * ((k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys) > (1LL << 30))
         return DSA_ERR_INVALID_ARG;
     if (dtype == DSA_F32 && R > 65535) return DSA_ERR_UNSUPPORTED;
+    // the tensor-core kernel addresses cache rows and q rows with int32
+    if (static_cast<long long>(R) * N >= (1LL << 31) || static_cast<long long>(R) * H >= (1LL << 31))
+        return DSA_ERR_INVALID_ARG;
     return DSA_OK;
 }
 

@@ -1,6 +1,7 @@
 // Internal interface between the host API (dsa_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,7 +20,9 @@ constexpr size_t kPartialFloats = static_cast<size_t>(kHeadsPad) * kD + 2 * kHea
 
 // One launch of the tensor-core kernel.  A unit is (row, key chunk): keys
 // [chunk * chunk_keys, min((chunk + 1) * chunk_keys, n_sel)) of one row.
+// launch_tc() fills tmap_q from q, R and H.
 struct TcParams {
+    CUtensorMap tmap_q;       // [R*H][512] bf16, box 64 x H, 128-byte swizzle
     const uint16_t* q;        // [R][H][512] bf16
     const uint16_t* kv;       // [N][512] or [R][N][512] bf16
     const int32_t* idx;       // [R][k_max]

@@ -82,6 +82,7 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv_cache) |
          reinterpret_cast<uintptr_t>(out)) & 15u)
         return DSA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * N >= (1LL << 31)) return DSA_ERR_INVALID_ARG;
     const long long chunks = (static_cast<long long>(k_max) + kDecodeChunkKeys - 1) / kDecodeChunkKeys;
     if (static_cast<long long>(B) * chunks > DSA_NOALLOC_MAX_UNITS) return DSA_ERR_UNSUPPORTED;
 

@@ -70,6 +70,50 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Arrive once on `bar` and add `bytes` to the transaction count its current
+// phase waits for (the TMA copies complete those bytes).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------- TMA
+// Four rows (row0..row3) of one 2-D tensor, columns [col, col + box width),
+// into consecutive box rows at dst; completion is counted on `bar`.  Rows
+// outside the tensor read as zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int col, int row0, int row1,
+                                            int row2, int row3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(col), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(bar)
+        : "memory");
+}
+
+// One box of a 2-D tensor starting at (col, row) into dst.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int col, int row,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(col), "r"(row), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = 0,
+// NaN stays NaN).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------------ cp.async
 // 16-byte global -> shared copy; src_bytes == 0 writes 16 zero bytes and
 // reads nothing.
@@ -129,6 +173,22 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// umma_bf16 with the operand descriptors given as a base plus compile-time
+// offsets (in 16-byte units), added inside the instruction sequence: the issue
+// loop stays a handful of instructions per MMA and nothing is hoisted.
+template <uint32_t kAOff, uint32_t kBOff>
+__device__ __forceinline__ void umma_bf16_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+        "add.u64 a, %1, %5;\n\t"
+        "add.u64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(kAOff), "n"(kBOff)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -148,6 +208,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// The value unchanged, but opaque to the compiler: keeps it from hoisting
+// many precomputed descriptors out of a loop (and spilling them).
+__device__ __forceinline__ uint64_t opaque64(uint64_t v) {
+    uint64_t r;
+    asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(v));
+    return r;
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an f32 accumulator.

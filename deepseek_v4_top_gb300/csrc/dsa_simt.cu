@@ -112,49 +112,45 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
     for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = acc[i] * f;
 }
 
-// One CTA per (row, group of 8 heads); thread t owns columns 4t .. 4t+3.
-// Partials of one row are merged in chunk order, so the result is
-// deterministic.  Each partial holds (m, l, O) with O and l relative to
-// 2^m (2^0 when m is -inf, in which case O and l are 0 or NaN).
+// One CTA per (row, head); thread t owns columns 4t .. 4t+3.  Partials of
+// one row are merged in chunk order, so the result is deterministic.  Each
+// partial holds (m, l, O) with O and l relative to 2^m (2^0 when m is -inf,
+// in which case O and l are 0 or NaN).
 __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p) {
-    const int r = blockIdx.x;
+    const int r = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x;
     const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
-    for (int hh = 0; hh < 8; ++hh) {
-        const int h = blockIdx.y * 8 + hh;
-        if (h >= p.H) break;
-        float M = -INFINITY;
-        bool have = false;
-        for (int c = 0; c < p.chunks; ++c) {
-            const float mc = ml_base[(static_cast<size_t>(r) * p.chunks + c) * 2 * kHeadsPad + h];
-            if (mc != -INFINITY) {
-                M = have ? fmaxf(M, mc) : mc;
-                have = true;
-            }
+    float M = -INFINITY;
+    bool have = false;
+    for (int c = 0; c < p.chunks; ++c) {
+        const float mc = ml_base[(static_cast<size_t>(r) * p.chunks + c) * 2 * kHeadsPad + h];
+        if (mc != -INFINITY) {
+            M = have ? fmaxf(M, mc) : mc;
+            have = true;
         }
-        const float mu = have ? M : 0.0f;
-        float l = 0.0f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < p.chunks; ++c) {
-            const size_t u = static_cast<size_t>(r) * p.chunks + c;
-            const float mc = ml_base[u * 2 * kHeadsPad + h];
-            const float lc = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
-            const float w = (mc == -INFINITY) ? 1.0f : exp2f(mc - mu);
-            l += w * lc;
-            const float4 o = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
-            acc.x = fmaf(w, o.x, acc.x);
-            acc.y = fmaf(w, o.y, acc.y);
-            acc.z = fmaf(w, o.z, acc.z);
-            acc.w = fmaf(w, o.w, acc.w);
-        }
-        const float s2 = p.sink[h] * kLog2e;
-        const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
-        const float e1 = exp2f(mu - mstar);
-        const float e2 = exp2f(s2 - mstar);
-        const float f = e1 / (l * e1 + e2);
-        float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
-        reinterpret_cast<float4*>(p.out + (static_cast<size_t>(r) * p.H + h) * kD)[tid] = res;
     }
+    const float mu = have ? M : 0.0f;
+    float l = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < p.chunks; ++c) {
+        const size_t u = static_cast<size_t>(r) * p.chunks + c;
+        const float mc = ml_base[u * 2 * kHeadsPad + h];
+        const float lc = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
+        const float w = (mc == -INFINITY) ? 1.0f : exp2f(mc - mu);
+        l += w * lc;
+        const float4 o = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+    }
+    const float s2 = p.sink[h] * kLog2e;
+    const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
+    const float e1 = exp2f(mu - mstar);
+    const float e2 = exp2f(s2 - mstar);
+    const float f = e1 / (l * e1 + e2);
+    float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+    reinterpret_cast<float4*>(p.out + (static_cast<size_t>(r) * p.H + h) * kD)[tid] = res;
 }
 
 }  // namespace
@@ -166,7 +162,7 @@ cudaError_t launch_simt(const SimtParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-    dim3 grid(p.R, (p.H + 7) / 8);
+    dim3 grid(p.R, p.H);
     dsa_combine_kernel<<<grid, 128, 0, s>>>(p);
     return cudaGetLastError();
 }

@@ -19,7 +19,7 @@ Conventions
 * ``q``    : [R, H, 512]  float32 array, or uint16 array of bf16 bits.
 * ``kv``   : prefill [N, 512], decode [B, N, 512] (slot b is row b's cache).
 * ``idx``  : int32 [R, k_max]; entries at and beyond ``n_sel[r]`` hold the
-             poison value -1 and must never be read.
+             poison value -1 and must never be used.
 * ``n_sel``: int32 [R].
 * ``sink`` : float32 [H].
 * ``scale``: python float (1/sqrt(512) unless a case says otherwise).

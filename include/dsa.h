@@ -23,7 +23,8 @@
  *     q     [R][H][512]    dtype (float32, or bfloat16 bit patterns)
  *     kv    prefill: [N][512] (one cache shared by all rows)
  *           decode:  [B][N][512] (row b reads only slot b)
- *     idx   [R][k_max] int32; only the first n_sel[r] entries are read
+ *     idx   [R][k_max] int32; only the first n_sel[r] entries are used (the
+ *           rest may be read ahead but are ignored; they need no valid value)
  *     n_sel [R] int32
  *     sink  [H] float32 (any value, including +-inf)
  *     out   [R][H][512] float32; must not overlap any input
