@@ -10,16 +10,26 @@
 // key chunk of a row when a decode batch is split across SMs).  Per 128-key
 // tile the work is a chain: gather -> scores -> softmax -> P.V, and the one
 // shared-memory KV tile (128 KiB) is busy from its gather to the end of its
-// P.V.  Eight worker warps therefore do every CUDA-core step in turn, so that
-// each step runs on all of them:
+// P.V.  Sixteen warps in four warpgroups:
 //
-//   * gather: 16-byte cp.async of whole 1 KiB rows (each thread copies 16
+//   * worker warps 0-7 (184 registers each, by setmaxnreg):
+//     gather: 16-byte cp.async of whole 1 KiB rows (each thread copies 16
 //     bytes of each 128-byte column segment, back to back) straight into a
-//     128-byte-swizzled tile of 8 segments x 128 keys x 64 columns.  The tile
-//     is read once from global memory and serves every head, as keys and as
-//     values.  Q arrives by tiled TMA.  Keys past n_sel are zero-filled;
-//     an out-of-range selection gathers a NaN row.
-//   * MMA warp 8 (one thread) issues tcgen05.mma:
+//     128-byte-swizzled tile of 8 segments x 128 keys x 64 columns, 32 keys
+//     at a time as the previous tile's P.V releases them.  The tile is read
+//     once from global memory and serves every head, as keys and as values.
+//     The tile's indices arrive one tile ahead by cp.async, Q by tiled TMA.
+//     Keys past n_sel are zero-filled; an out-of-range selection gathers a
+//     NaN row.
+//     softmax: worker w reads TMEM lane quadrant w%4 (32 keys) and heads
+//     32*(w/4) .. +31.  A unit's first tile sets per-head reference maxima
+//     (warp transpose reduction, one sync).  Later tiles use them
+//     optimistically; a score more than 2^8 above its reference flags the
+//     tile and the MMA warp has it redone with moved references (running
+//     sums and O^T rescaled).  Weights are written as two bf16 terms
+//     (P = hi + lo) so the value sum keeps ~14 bits; each thread keeps its
+//     key lane's running sums, reduced over the 128 lanes once per unit.
+//   * MMA warp 12 (one thread) issues tcgen05.mma:
 //       S^T[key][head]  = KV_tile (K-major, M=128) x Q^T (K-major, N=64)
 //       O^T[col][head] += V^T (MN-major, M=128 per 128 columns) x P^T
 //     P^T is one N=128 operand [P_hi | P_lo] for three of the four 128-column
@@ -27,15 +37,9 @@
 //     thirds) and two N=64 operands for the fourth, so the accumulators fit
 //     TMEM: S^T columns [0,64), O^T chunks 0-2 at [64,192), [192,320),
 //     [320,448) (hi | lo halves), chunk 3 at [448,512).
-//   * softmax: worker w reads TMEM lane quadrant w%4 (32 keys) and heads
-//     32*(w/4) .. +31.  A per-head reference maximum moves only when a score
-//     exceeds it by more than 2^8 (then the running sums and O^T are
-//     rescaled); only then are the tile maxima reduced (warp-shuffle
-//     transpose reduction).  Weights are written as two bf16 terms
-//     (P = hi + lo) so the value sum keeps ~16 bits; each thread keeps its
-//     key lane's running sums, reduced over the 128 lanes once per unit.
-//   * epilogue: sink fold and fp32 store, overlapped with the next tile's
-//     gather and scores.
+//   * output warps 8-11 (one per TMEM lane quadrant): sink fold and fp32
+//     store of a finished unit while the workers run the next one; the next
+//     unit's first P.V waits until they have read O^T.
 //
 // Every wait is bounded (see dsa_ptx.cuh); on a timeout the kernel raises an
 // error bit, lets its copies land, frees its TMEM and returns.
@@ -53,10 +57,22 @@
 namespace dsa {
 namespace {
 
+// Four warpgroups: two of worker warps, one of output warps (one per TMEM
+// lane quadrant), one holding the MMA warp.  The launch gives every thread
+// 128 registers; the workers take 184 and the others keep 72.
 constexpr int kWorkerWarps = 8;
 constexpr int kWorkers = 32 * kWorkerWarps;
-constexpr int kMmaWarp = kWorkerWarps;
-constexpr int kThreads = kWorkers + 32;
+constexpr int kOutWarp0 = 8;
+constexpr int kOutWarps = 4;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 512;
+constexpr int kIdxWarp = kWorkerWarps - 1;   // copies each tile's indices ahead
+constexpr uint32_t kRegsWorker = 184;
+constexpr uint32_t kRegsOther = 72;
+// two warpgroups at kRegsWorker and two at kRegsOther use exactly the
+// 65536 registers that 512 threads x 128 bring
+static_assert((2 * kRegsWorker + 2 * kRegsOther) * 128 == 65536 && 65536 / kThreads == 128,
+              "the register split must add up to what the launch provides");
 constexpr float kTau = 8.0f;            // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -79,26 +95,34 @@ __host__ __device__ constexpr uint32_t tmem_o(int i) { return 64u + 128u * stati
 
 struct Misc {
     uint64_t kv_full;       // workers' cp.async -> MMA: the KV tile landed
-    uint64_t kv_free;       // MMA -> workers: P.V of the tile done (buffer and O^T free)
+    uint64_t kv_free[4];    // MMA -> workers: P.V is done with keys [0, 32(i+1)) of the
+                            // tile; [3]: with the whole buffer and O^T
     uint64_t s_full;        // MMA -> workers: scores of the tile ready
-    uint64_t p_full;        // workers -> MMA: P written (and O^T rescaled)
+    uint64_t p_full;        // worker warps -> MMA: P written (and O^T rescaled)
     uint64_t q_full;        // Q TMA -> MMA: Q of the unit landed
     uint64_t q_free;        // MMA -> worker 0: last score MMA of the unit done
-    uint64_t grp[3];        // worker-group syncs
+    uint64_t p_ack;         // MMA -> workers: P accepted, or ms.redo set
+    uint64_t red_sync;      // worker-warp sync of the tile-maxima reduction (one arrival per warp)
     uint64_t drain;         // MMA thread: everything it issued completed
-    // the arrays below are read as float2 / float4: keep them 16-byte aligned
-    alignas(16) float red_max[4][64];   // [TMEM lane quadrant][head]
-    alignas(16) float red_sum[4][64];
+    uint64_t idx_full;      // index warp's cp.async -> workers: idx[] holds the next tile's
+    uint64_t o_full;        // MMA -> output warps: the unit's last P.V is done
+    uint64_t o_free;        // output warps -> MMA: the unit's O^T has been read
+    uint64_t l_ready;       // worker warps -> output warps: red_l, m_ref hold the unit's sums, maxima
+    uint64_t l_free;        // output warps -> workers: red_l, m_ref of the unit have been read
+    // the arrays below are read as float4: keep them 16-byte aligned
+    alignas(16) float red[4][64];       // [TMEM lane quadrant][head]: tile maxima
+    alignas(16) float red_l[4][64];     // [TMEM lane quadrant][head]: a finished unit's sums
     alignas(16) float m_ref[64];        // per-head reference maximum (log2 units)
-    alignas(16) float alpha[64];        // per-head rescale factor; epilogue: output factor
     int ovf[kWorkerWarps];              // per worker warp: a score passed its reference max
     uint32_t tmem_base;
     int abort_flag;
-    int rescale_flag;
+    int redo;                           // the flagged tile is to be redone
+    int idx[128];                       // the selected rows of the tile being gathered
+    int idx_nsel;                       // n_sel of that tile's query row
 };
 
-static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0 &&
-                  offsetof(Misc, m_ref) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
+static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, red_l) % 16 == 0 &&
+                  offsetof(Misc, m_ref) % 16 == 0,
               "vector-accessed arrays must be 16-byte aligned");
 static_assert(kOffMisc % 16 == 0, "Misc must start 16-byte aligned");
 constexpr size_t kSmemBytes = kOffMisc + ((sizeof(Misc) + 15) / 16) * 16;
@@ -132,9 +156,12 @@ __device__ __forceinline__ Unit unit_info(const TcParams& p, int u) {
     return unit_from(p, u, __ldg(p.n_sel + u / p.chunks));
 }
 
+// Sync of the worker warps: one arrival per warp (after __syncwarp, which
+// orders the lanes' shared-memory writes before lane 0's release).
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t& phase, volatile int* ab,
                                            uint32_t* err) {
-    mbar_arrive(bar);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
     const bool ok = mbar_wait(bar, phase, ab, err);
     phase ^= 1u;
     return ok;
@@ -169,40 +196,38 @@ __device__ __forceinline__ float warp_transpose_reduce32(float* v, int lane) {
 }
 
 // ------------------------------------------------------------------ gather
-// The indices of this worker thread's four rows of a tile, loaded ahead
-// without being looked at (so the loads do not stall the thread), and the
-// n_sel of the tile's row.  Worker thread (warp w, lane l) copies 16 bytes
-// (column chunk l%8) of each 128-byte segment of rows j = 4*(w + 8q) + l/8.
-struct Prefetch {
-    int raw[4];
-    int nsel;
-};
-
-__device__ __forceinline__ Prefetch prefetch_rows(const TcParams& p, int u, int t, int wt) {
-    const int w = wt >> 5, lane = wt & 31;
+// The index warp copies the 128 selected rows of a tile (and its row's
+// n_sel) into shared memory with cp.async while the previous tile is being
+// computed, so that no thread holds them in registers meanwhile.  Entries at
+// or past k_max are never read.
+__device__ __forceinline__ void prefetch_idx(const TcParams& p, int u, int t, Misc& ms, int lane) {
     const int r = u / p.chunks, c = u - r * p.chunks;
-    Prefetch f;
-    f.nsel = __ldg(p.n_sel + r);
+    const int* row = p.idx + static_cast<size_t>(r) * p.k_max;
+    const int k0 = c * p.chunk_keys + t * 128;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int kk = c * p.chunk_keys + t * 128 + 4 * (w + 8 * q) + (lane >> 3);
-        f.raw[q] = kk < p.k_max ? __ldg(p.idx + static_cast<size_t>(r) * p.k_max + kk) : 0;
+    for (int i = 0; i < 4; ++i) {
+        const int kk = k0 + lane + 32 * i;
+        const bool in = kk < p.k_max;
+        cp_async4(smem_addr(&ms.idx[lane + 32 * i]), in ? row + kk : row, in ? 4u : 0u);
     }
-    return f;
+    if (lane == 0) cp_async4(smem_addr(&ms.idx_nsel), p.n_sel + r, 4u);
+    cp_async_arrive(smem_addr(&ms.idx_full));
 }
 
-// Validate the prefetched indices against the unit and copy the rows: keys
+// Validate the prefetched indices against the unit and copy rows [32q,
+// 32q + 32) of the tile: worker thread (warp w, lane l) copies 16 bytes
+// (column chunk l%8) of each 128-byte segment of row 4*(w + 8q) + l/8.  Keys
 // past n_valid are zero-filled, an out-of-range selection copies a NaN row.
-__device__ __forceinline__ void issue_rows(const TcParams& p, const Prefetch& f, const Unit& un, int t,
+template <int q>
+__device__ __forceinline__ void issue_rows(const TcParams& p, const Misc& ms, const Unit& un, int t,
                                           uint32_t sKv, int wt) {
     const int w = wt >> 5, lane = wt & 31, cc = lane & 7;
     const uint16_t* cache = p.kv + (p.decode ? static_cast<size_t>(un.r) * p.N * kD : 0);
     const uint16_t* nan_row = reinterpret_cast<const uint16_t*>(kNanRowBf16);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    {
         const int j = 4 * (w + 8 * q) + (lane >> 3);
         const bool valid = t * 128 + j < un.n_valid;
-        const int id = f.raw[q];
+        const int id = ms.idx[j];
         const bool in_range = !un.bad_n && id >= 0 && id < p.N;
         if (valid && !un.bad_n && !in_range && cc == 0) atomicOr(p.err, DSA_DEVERR_IDX_RANGE);
         const uint16_t* sp = (in_range ? cache + static_cast<size_t>(id) * kD : nan_row) + cc * 8;
@@ -228,34 +253,31 @@ __device__ __forceinline__ void score_mmas(uint32_t d, uint64_t dKv, uint64_t dQ
     score_mma_step<0>(d, dKv, dQ);
 }
 
-// O^T += V^T x P^T for one 128-column chunk with the stacked N=128 operand.
-template <int i, int kk>
-__device__ __forceinline__ void pv128_step(uint32_t tmem, uint64_t dV, uint64_t dPst, uint32_t acc0) {
-    constexpr uint32_t idPV128 = idesc_bf16(128, 128, true, true);
-    constexpr uint32_t aoff = (2 * i * kSegBytes + kk * 2048) >> 4;
-    constexpr uint32_t boff = (kk * 2048) >> 4;
-    umma_bf16_at<aoff, boff>(tmem + tmem_o(i), dV, dPst, idPV128, acc0 | kk);
-    if constexpr (kk + 1 < 8) pv128_step<i, kk + 1>(tmem, dV, dPst, acc0);
-}
-
-// Chunk 3: two N=64 operands (P_hi, P_lo) into one 64-column accumulator.
+// O^T += V^T x P^T for 16 keys (k-step kk) of every 128-column chunk: the
+// stacked N=128 operand for chunks 0-2, two N=64 operands for chunk 3.
 template <int kk>
-__device__ __forceinline__ void pv64_step(uint32_t tmem, uint64_t dV, uint64_t dPhi, uint64_t dPlo,
-                                          uint32_t acc0) {
+__device__ __forceinline__ void pv_kstep(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi, uint64_t dPlo,
+                                         uint32_t acc0) {
+    constexpr uint32_t idPV128 = idesc_bf16(128, 128, true, true);
     constexpr uint32_t idPV64 = idesc_bf16(128, 64, true, true);
-    constexpr uint32_t aoff = (6 * kSegBytes + kk * 2048) >> 4;
     constexpr uint32_t boff = (kk * 2048) >> 4;
-    umma_bf16_at<aoff, boff>(tmem + tmem_o(3), dV, dPhi, idPV64, acc0 | kk);
-    umma_bf16_at<aoff, boff>(tmem + tmem_o(3), dV, dPlo, idPV64, 1u);
-    if constexpr (kk + 1 < 8) pv64_step<kk + 1>(tmem, dV, dPhi, dPlo, acc0);
+    constexpr uint32_t a0 = (0 * kSegBytes + kk * 2048) >> 4, a1 = (2 * kSegBytes + kk * 2048) >> 4;
+    constexpr uint32_t a2 = (4 * kSegBytes + kk * 2048) >> 4, a3 = (6 * kSegBytes + kk * 2048) >> 4;
+    umma_bf16_at<a0, boff>(tmem + tmem_o(0), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a1, boff>(tmem + tmem_o(1), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a2, boff>(tmem + tmem_o(2), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPhi, idPV64, acc0 | kk);
+    umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPlo, idPV64, 1u);
 }
 
-__device__ __forceinline__ void pv_mmas(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi,
-                                        uint64_t dPlo, uint32_t acc0) {
-    pv128_step<0, 0>(tmem, dV, dPst, acc0);
-    pv128_step<1, 0>(tmem, dV, dPst, acc0);
-    pv128_step<2, 0>(tmem, dV, dPst, acc0);
-    pv64_step<0>(tmem, dV, dPhi, dPlo, acc0);
+// Keys [32q, 32q + 32) of the tile, then a commit that frees those rows of
+// the KV buffer for the next tile's gather.
+template <int q>
+__device__ __forceinline__ void pv_quarter(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi,
+                                           uint64_t dPlo, uint32_t acc0, Misc& ms) {
+    pv_kstep<2 * q>(tmem, dV, dPst, dPhi, dPlo, acc0);
+    pv_kstep<2 * q + 1>(tmem, dV, dPst, dPhi, dPlo, acc0);
+    umma_commit(smem_addr(&ms.kv_free[q]));
 }
 
 __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem) {
@@ -272,6 +294,7 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
     const uint64_t dPhi = sdesc_sw128(sPhi, 1024, 1024);
     const uint64_t dPlo = sdesc_sw128(sPlo, 1024, 1024);
     int g = 0, nu = 0;
+    uint32_t ph_p = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
         const Unit un = unit_info(p, u);
         if (!mbar_wait(smem_addr(&ms.q_full), nu & 1, ab, p.err)) return;
@@ -285,10 +308,32 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
             if (t == un.tiles - 1) umma_commit(smem_addr(&ms.q_free));
 
             // values: O^T[col][head] += V^T x (P_hi + P_lo)^T, 128 columns at a time
-            if (!mbar_wait(smem_addr(&ms.p_full), g & 1, ab, p.err)) return;
+            if (!mbar_wait(smem_addr(&ms.p_full), ph_p, ab, p.err)) return;
+            ph_p ^= 1u;
+            // a tile that a worker warp flagged is redone with new reference maxima
+            volatile int* ovf = ms.ovf;
+            int flagged = 0;
+#pragma unroll
+            for (int w = 0; w < kWorkerWarps; ++w) flagged |= ovf[w];
+            if (flagged) {
+#pragma unroll
+                for (int w = 0; w < kWorkerWarps; ++w) ovf[w] = 0;
+                *reinterpret_cast<volatile int*>(&ms.redo) = 1;
+                mbar_arrive(smem_addr(&ms.p_ack));
+                if (!mbar_wait(smem_addr(&ms.p_full), ph_p, ab, p.err)) return;
+                ph_p ^= 1u;
+                *reinterpret_cast<volatile int*>(&ms.redo) = 0;
+            }
+            mbar_arrive(smem_addr(&ms.p_ack));
+            // a unit's first P.V overwrites O^T: the output warps must have read the last one
+            if (t == 0 && nu > 0 && !mbar_wait(smem_addr(&ms.o_free), (nu - 1) & 1, ab, p.err)) return;
             tc_fence_after();
-            pv_mmas(tmem, dV, dPst, dPhi, dPlo, t > 0 ? 1u : 0u);
-            umma_commit(smem_addr(&ms.kv_free));
+            const uint32_t acc0 = t > 0 ? 1u : 0u;
+            pv_quarter<0>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<1>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<2>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<3>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            if (t == un.tiles - 1) umma_commit(smem_addr(&ms.o_full));
         }
     }
 }
@@ -297,174 +342,78 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
 struct WorkerCtx {
     int wt, w, lane, qd, hf, key;   // thread, warp, lane, TMEM lane quadrant, head half, key in tile
     uint32_t lane_off;
-    uint32_t ph[3];
+    uint32_t ph_red, ph_ack;        // phases of red_sync and p_ack
 };
 
-// Per-head sums over the 128 key lanes, sink fold, store of one finished unit.
-__device__ __forceinline__ bool epilogue(const TcParams& p, Misc& ms, WorkerCtx& c, uint32_t tmem, int u,
-                                         int r, float* lacc /* clobbered */) {
-    volatile int* ab = &ms.abort_flag;
-    ms.red_sum[c.qd][32 * c.hf + c.lane] = warp_transpose_reduce32<false>(lacc, c.lane);
-    if (!group_sync(smem_addr(&ms.grp[1]), c.ph[1], ab, p.err)) return false;
-    if (c.w == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 2 * c.lane + e;
-            const float l = (ms.red_sum[0][h] + ms.red_sum[1][h]) + (ms.red_sum[2][h] + ms.red_sum[3][h]);
-            const float m = ms.m_ref[h];
-            float f = 1.0f;
-            if (!p.partial) {
-                const float mu = m == -INFINITY ? 0.0f : m;
-                const float s2 = h < p.H ? __ldg(p.sink + h) * kLog2e : 0.0f;
-                const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
-                const float e1 = exp2f(mu - mstar);
-                const float e2 = exp2f(s2 - mstar);
-                f = e1 / (l * e1 + e2);
-            } else {
-                float* ml = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD +
-                            static_cast<size_t>(u) * 2 * kHeadsPad;
-                ml[h] = m;
-                ml[kHeadsPad + h] = l;
-            }
-            ms.alpha[h] = f;
-            ms.m_ref[h] = -INFINITY;          // the next unit starts afresh
-        }
-    }
-    if (!group_sync(smem_addr(&ms.grp[0]), c.ph[0], ab, p.err)) return false;
-    tc_fence_after();
-    float* dst = p.partial ? p.part + static_cast<size_t>(u) * kHeadsPad * kD
-                           : p.out + static_cast<size_t>(r) * p.H * kD;
-    // four chunks of this thread's column x its 32 heads; chunks 0-2 add the lo half
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t ta = tmem + c.lane_off + tmem_o(i) + 32 * c.hf;
-        float o[32];
-        tmem_ld32(ta, o);
-        if (i < 3) {
-            float lo[32];
-            tmem_ld32(ta + 64, lo);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) o[h] += lo[h];
-        }
-        const int d = i * 128 + c.key;
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 f = *reinterpret_cast<const float4*>(&ms.alpha[32 * c.hf + 4 * h4]);
-            const float ff[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int h = 32 * c.hf + 4 * h4 + e;
-                if (h < p.H) dst[static_cast<size_t>(h) * kD + d] = o[4 * h4 + e] * ff[e];
-            }
-        }
-    }
-    return true;
-}
-
-// Softmax of one tile: weights into P (hi, lo), running sums into lacc.
-__device__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerCtx& c, uint32_t tmem,
-                             const Unit& un, int t, float* lacc) {
-    volatile int* ab = &ms.abort_flag;
-    const uint32_t ts = tmem + c.lane_off + kTmemS + 32 * c.hf;
-    const bool valid = t * 128 + c.key < un.n_valid;
-    const float sc = p.scale_log2;
-    const float* mref = &ms.m_ref[32 * c.hf];
-
-    float x[32];
+// Scores of this thread's key for its 32 heads, in log2 units; -inf for a
+// key past n_valid.
+__device__ __forceinline__ void load_scores(uint32_t ts, bool valid, float sc, float* x) {
     tmem_ld32(ts, x);
 #pragma unroll
     for (int h = 0; h < 32; ++h) x[h] = valid ? x[h] * sc : -INFINITY;
+}
 
-    // Does any score exceed its head's reference maximum by more than 2^8?
-    // (The reference is -inf at the start of a unit, so any finite score
-    // does.)  Only then are the tile maxima reduced.
-    bool ovf = false;
+// New reference maxima for this thread's 32 heads from the tile maxima of
+// all four key quadrants (one sync of the worker warps).  On a unit's first
+// tile the references are set; later a reference moves only when the tile
+// maximum passes it by more than 2^kTau, and then this thread's running sums
+// and its block of O^T are rescaled.  The quadrant-0 warps publish the new
+// references for later tiles and for the output warps.  x is clobbered.
+template <bool kFirst>
+__device__ bool new_reference(const TcParams& p, Misc& ms, WorkerCtx& c, uint32_t tmem, float* x,
+                              float* mref, int nu, float* lacc) {
+    volatile int* ab = &ms.abort_flag;
+    // lane l: head l's maximum over this warp's 32 keys
+    ms.red[c.qd][32 * c.hf + c.lane] = warp_transpose_reduce32<true>(x, c.lane);
+    if (!group_sync(smem_addr(&ms.red_sync), c.ph_red, ab, p.err)) return false;
+    if (c.qd == 0) {
+        // lane l publishes head l's reference (read by later tiles and the
+        // output warps, which may still be reading the previous unit's)
+        if (kFirst && nu > 0 && !mbar_wait(smem_addr(&ms.l_free), (nu - 1) & 1, ab, p.err)) return false;
+        const int h = 32 * c.hf + c.lane;
+        const float tm = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+        if (kFirst) {
+            ms.m_ref[h] = tm;
+        } else {
+            const float mo = ms.m_ref[h];
+            if (mo == -INFINITY || tm > mo + kTau) ms.m_ref[h] = tm;
+        }
+    }
+    bool resc = false;           // the same in every lane: the warp's lanes share their heads
+    float alpha[32];
 #pragma unroll
     for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(&mref[4 * h4]);
-        ovf |= (x[4 * h4] > m4.x + kTau) | (x[4 * h4 + 1] > m4.y + kTau) | (x[4 * h4 + 2] > m4.z + kTau) |
-               (x[4 * h4 + 3] > m4.w + kTau);
-    }
-    ovf = __any_sync(0xffffffffu, ovf);
-    if (c.lane == 0) ms.ovf[c.w] = ovf ? 1 : 0;
-    if (!group_sync(smem_addr(&ms.grp[0]), c.ph[0], ab, p.err)) return false;
-    int any_ovf = 0;
+        const float4 q0 = *reinterpret_cast<const float4*>(&ms.red[0][32 * c.hf + 4 * h4]);
+        const float4 q1 = *reinterpret_cast<const float4*>(&ms.red[1][32 * c.hf + 4 * h4]);
+        const float4 q2 = *reinterpret_cast<const float4*>(&ms.red[2][32 * c.hf + 4 * h4]);
+        const float4 q3 = *reinterpret_cast<const float4*>(&ms.red[3][32 * c.hf + 4 * h4]);
+        const float tm[4] = {fmaxf(fmaxf(q0.x, q1.x), fmaxf(q2.x, q3.x)), fmaxf(fmaxf(q0.y, q1.y), fmaxf(q2.y, q3.y)),
+                             fmaxf(fmaxf(q0.z, q1.z), fmaxf(q2.z, q3.z)), fmaxf(fmaxf(q0.w, q1.w), fmaxf(q2.w, q3.w))};
 #pragma unroll
-    for (int w = 0; w < kWorkerWarps; ++w) any_ovf |= ms.ovf[w];
-    if (any_ovf) {
-        ms.red_max[c.qd][32 * c.hf + c.lane] = warp_transpose_reduce32<true>(x, c.lane);
-        // the reduction clobbered x: read the scores again
-        tmem_ld32(ts, x);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) x[h] = valid ? x[h] * sc : -INFINITY;
-        if (!group_sync(smem_addr(&ms.grp[1]), c.ph[1], ab, p.err)) return false;
-        if (c.w == 0) {
-            bool resc = false;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int h = 2 * c.lane + e;
-                const float tm = fmaxf(fmaxf(ms.red_max[0][h], ms.red_max[1][h]),
-                                       fmaxf(ms.red_max[2][h], ms.red_max[3][h]));
-                const float mo = ms.m_ref[h];
-                float mn = mo, al = 1.0f;
-                if (mo == -INFINITY) {
-                    mn = tm;                       // nothing weighted yet
-                } else if (tm > mo + kTau) {
-                    mn = tm;
-                    al = exp2f(mo - mn);
-                    resc = true;
-                }
-                ms.m_ref[h] = mn;
-                ms.alpha[h] = al;
+        for (int e = 0; e < 4; ++e) {
+            const int h = 4 * h4 + e;
+            if (kFirst) {
+                mref[h] = tm[e];
+                continue;
             }
-            const bool any = __any_sync(0xffffffffu, resc);
-            if (c.lane == 0) ms.rescale_flag = any ? 1 : 0;
-        }
-        if (!group_sync(smem_addr(&ms.grp[2]), c.ph[2], ab, p.err)) return false;
-        if (ms.rescale_flag) {
-            // a moved reference maximum rescales the running sums (O^T below)
-            const float* al = &ms.alpha[32 * c.hf];
-#pragma unroll
-            for (int h = 0; h < 32; ++h) lacc[h] *= al[h];
-        }
-    }
-
-    // weights relative to the reference maximum (0 when it is -inf)
-#pragma unroll
-    for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(&mref[4 * h4]);
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float mu = mm[e] == -INFINITY ? 0.0f : mm[e];
-            const float pe = ex2_approx(x[4 * h4 + e] - mu);
-            x[4 * h4 + e] = pe;
-            lacc[4 * h4 + e] += pe;
+            const float mo = mref[h];
+            float mn = mo, al = 1.0f;
+            if (mo == -INFINITY) {
+                mn = tm[e];                    // nothing weighted yet
+            } else if (tm[e] > mo + kTau) {
+                mn = tm[e];
+                al = exp2f(mo - mn);
+                resc = true;
+            }
+            mref[h] = mn;
+            alpha[h] = al;
         }
     }
-    // P = hi + lo, both bf16: this key's row, this thread's 4 chunks of 8 heads
-    uint8_t* prow_hi = smem + kOffPhi + c.key * 128;
-    uint8_t* prow_lo = smem + kOffPlo + c.key * 128;
+    if (!kFirst && resc) {
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = x[8 * c4 + 2 * e], b = x[8 * c4 + 2 * e + 1];
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(a, b);
-            const float2 hf = __bfloat1622float2(hv);
-            const __nv_bfloat162 lv = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-            hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
-            lw[e] = *reinterpret_cast<const uint32_t*>(&lv);
-        }
-        const int pc = ((4 * c.hf + c4) ^ (c.key & 7)) << 4;
-        *reinterpret_cast<uint4*>(prow_hi + pc) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(prow_lo + pc) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    if (any_ovf && ms.rescale_flag) {
-        // ... and what P.V accumulated so far (that P.V finished before this
-        // tile's gather was issued); before P_full, so before this tile's P.V
-        const float* al = &ms.alpha[32 * c.hf];
+        for (int h = 0; h < 32; ++h) lacc[h] *= alpha[h];
+        // O^T of the earlier tiles (their P.V is complete: this tile's gather
+        // waited for it), before this tile's P.V
         tc_fence_after();
 #pragma unroll 1
         for (int i = 0; i < 7; ++i) {     // chunks 0-2: hi and lo halves; chunk 3
@@ -472,13 +421,95 @@ __device__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerC
             float o[32];
             tmem_ld32(ta, o);
 #pragma unroll
-            for (int h = 0; h < 32; ++h) o[h] *= al[h];
+            for (int h = 0; h < 32; ++h) o[h] *= alpha[h];
             tmem_st32(ta, o);
         }
     }
+    return true;
+}
+
+// Weights relative to the references (0 when a reference is -inf) replace
+// the scores in x and are written to P as two bf16 terms: hi is the top 16
+// bits of the fp32 weight, lo the top 16 bits of the exact remainder, so
+// hi + lo is within 2^-14 of the weight (relative) and the split takes no
+// conversion instructions.  This key's row, this thread's 4 chunks of 8 heads.
+__device__ __forceinline__ void write_p(uint8_t* smem, const WorkerCtx& c, float* x, const float* mref) {
+#pragma unroll
+    for (int h = 0; h < 32; ++h) {
+        const float mu = mref[h] == -INFINITY ? 0.0f : mref[h];
+        x[h] = ex2_approx(x[h] - mu);
+    }
+    uint8_t* prow_hi = smem + kOffPhi + c.key * 128;
+    uint8_t* prow_lo = smem + kOffPlo + c.key * 128;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t ua = __float_as_uint(x[8 * c4 + 2 * e]);
+            const uint32_t ub = __float_as_uint(x[8 * c4 + 2 * e + 1]);
+            const float la = x[8 * c4 + 2 * e] - __uint_as_float(ua & 0xFFFF0000u);
+            const float lb = x[8 * c4 + 2 * e + 1] - __uint_as_float(ub & 0xFFFF0000u);
+            hw[e] = __byte_perm(ua, ub, 0x7632);     // head 2e in the low half, 2e+1 in the high
+            lw[e] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
+        }
+        const int pc = ((4 * c.hf + c4) ^ (c.key & 7)) << 4;
+        *reinterpret_cast<uint4*>(prow_hi + pc) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(prow_lo + pc) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
+// P (and any O^T rescale) done: hand the tile to the MMA warp and wait for its
+// answer, which says whether a flagged tile has to be redone.
+__device__ __forceinline__ bool publish_p(const TcParams& p, Misc& ms, WorkerCtx& c) {
     fence_proxy_async();
     tc_fence_before();
-    mbar_arrive(smem_addr(&ms.p_full));
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(smem_addr(&ms.p_full));
+    if (!mbar_wait(smem_addr(&ms.p_ack), c.ph_ack, &ms.abort_flag, p.err)) return false;
+    c.ph_ack ^= 1u;
+    return true;
+}
+
+// Softmax of one tile: weights into P, running sums into lacc.  Later tiles
+// use the current references optimistically; a warp that sees a score more
+// than 2^kTau above its reference flags the tile, and the MMA warp then has
+// every worker redo it with new references before any P.V reads P.
+__device__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerCtx& c, uint32_t tmem,
+                             const Unit& un, int t, int nu, float* lacc) {
+    const uint32_t ts = tmem + c.lane_off + kTmemS + 32 * c.hf;
+    const bool valid = t * 128 + c.key < un.n_valid;
+    float x[32], mref[32];
+    load_scores(ts, valid, p.scale_log2, x);
+    bool ovf = false;
+    if (t == 0) {
+        if (!new_reference<true>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
+        load_scores(ts, valid, p.scale_log2, x);
+    } else {
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(&ms.m_ref[32 * c.hf + 4 * h4]);
+            mref[4 * h4] = m4.x;
+            mref[4 * h4 + 1] = m4.y;
+            mref[4 * h4 + 2] = m4.z;
+            mref[4 * h4 + 3] = m4.w;
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) ovf |= x[h] > mref[h] + kTau;
+        ovf = __any_sync(0xffffffffu, ovf);
+    }
+    write_p(smem, c, x, mref);
+    if (ovf && c.lane == 0) ms.ovf[c.w] = 1;
+    if (!publish_p(p, ms, c)) return false;
+    if (ms.redo) {
+        load_scores(ts, valid, p.scale_log2, x);
+        if (!new_reference<false>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
+        load_scores(ts, valid, p.scale_log2, x);
+        write_p(smem, c, x, mref);
+        if (!publish_p(p, ms, c)) return false;
+    }
+#pragma unroll
+    for (int h = 0; h < 32; ++h) lacc[h] += x[h];
     return true;
 }
 
@@ -491,7 +522,7 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
     c.hf = c.w >> 2;
     c.key = 32 * c.qd + c.lane;
     c.lane_off = static_cast<uint32_t>(32 * c.qd) << 16;
-    c.ph[0] = c.ph[1] = c.ph[2] = 0u;
+    c.ph_red = c.ph_ack = 0u;
     volatile int* ab = &ms.abort_flag;
     const uint32_t sKv = smem_addr(smem + kOffKv);
     const uint32_t sQ = smem_addr(smem + kOffQ);
@@ -500,49 +531,48 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
 
     int u = blockIdx.x;
     if (u >= p.units) return;
-    Prefetch cur = prefetch_rows(p, u, 0, c.wt);
-    Unit un = unit_from(p, u, cur.nsel);
+    if (c.w == kIdxWarp) prefetch_idx(p, u, 0, ms, c.lane);
     if (q_thread) {
         const uint32_t bar = smem_addr(&ms.q_full);
         mbar_arrive_expect_tx(bar, q_bytes);
-        for (int s = 0; s < 8; ++s) tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, un.r * p.H, bar);
+        for (int s = 0; s < 8; ++s)
+            tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u / p.chunks) * p.H, bar);
         ++q_armed;
     }
+    Unit un;
     float lacc[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) lacc[h] = 0.0f;
     int t = 0, g = 0, nu = 0;
-    int prev_u = -1, prev_r = 0;
-    bool have_tile = true;
     while (true) {
-        // 1. the previous tile's P.V is done with the KV buffer (and O^T)
-        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free), (g - 1) & 1, ab, p.err)) return;
-        bool last_tile = false, more = false;
-        int u_next = u;
-        if (have_tile) {
-            // 2. gather this tile
-            if (t == 0 && un.bad_n && un.c == 0 && c.wt == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
-            issue_rows(p, cur, un, t, sKv, c.wt);
-            cp_async_arrive(smem_addr(&ms.kv_full));
-            last_tile = t + 1 == un.tiles;
-            u_next = last_tile ? u + static_cast<int>(gridDim.x) : u;
-            more = u_next < p.units;
-        }
-        // 3. finish the previous unit (its last P.V is done) while the gather
-        //    of this tile runs
-        if ((t == 0 || !have_tile) && prev_u >= 0) {
-            if (!epilogue(p, ms, c, tmem, prev_u, prev_r, lacc)) return;
-#pragma unroll
-            for (int h = 0; h < 32; ++h) lacc[h] = 0.0f;
-        }
-        if (!have_tile) break;
-        // 4. scores of this tile
+        // 1-2. gather this tile, 32 keys at a time, each as soon as the previous
+        //      tile's P.V is done with those rows of the buffer
+        if (!mbar_wait(smem_addr(&ms.idx_full), g & 1, ab, p.err)) return;
+        if (t == 0) un = unit_from(p, u, ms.idx_nsel);
+        if (t == 0 && un.bad_n && un.c == 0 && c.wt == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
+        const uint32_t ph = (g - 1) & 1;
+        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[0]), ph, ab, p.err)) return;
+        issue_rows<0>(p, ms, un, t, sKv, c.wt);
+        cp_async_arrive(smem_addr(&ms.kv_full));
+        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[1]), ph, ab, p.err)) return;
+        issue_rows<1>(p, ms, un, t, sKv, c.wt);
+        cp_async_arrive(smem_addr(&ms.kv_full));
+        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[2]), ph, ab, p.err)) return;
+        issue_rows<2>(p, ms, un, t, sKv, c.wt);
+        cp_async_arrive(smem_addr(&ms.kv_full));
+        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[3]), ph, ab, p.err)) return;
+        issue_rows<3>(p, ms, un, t, sKv, c.wt);
+        cp_async_arrive(smem_addr(&ms.kv_full));
+        const bool last_tile = t + 1 == un.tiles;
+        const int u_next = last_tile ? u + static_cast<int>(gridDim.x) : u;
+        const bool more = u_next < p.units;
+        // 3. scores of this tile
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) return;
         tc_fence_after();
-        // 5. indices of the next tile, loaded while the weights are computed
-        //    (global loads running beside the score MMAs slow them down)
-        if (more) cur = prefetch_rows(p, u_next, last_tile ? 0 : t + 1, c.wt);
-        // 6. weights
+        // 4. indices of the next tile, copied while the weights are computed
+        //    (every thread has issued this tile's gather: idx[] is free)
+        if (more && c.w == kIdxWarp) prefetch_idx(p, u_next, last_tile ? 0 : t + 1, ms, c.lane);
+        // 5. weights
         if (last_tile && more && q_thread) {
             // the unit's last score MMA has read Q: load the next unit's
             if (!mbar_wait(smem_addr(&ms.q_free), nu & 1, ab, p.err)) return;
@@ -552,19 +582,95 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
                 tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u_next / p.chunks) * p.H, bar);
             ++q_armed;
         }
-        if (!softmax_tile(p, smem, ms, c, tmem, un, t, lacc)) return;
+        if (!softmax_tile(p, smem, ms, c, tmem, un, t, nu, lacc)) return;
         ++g;
-        if (last_tile) {
-            prev_u = u;
-            prev_r = un.r;
-            ++nu;
-            have_tile = more;
-            u = u_next;
-            if (more) un = unit_from(p, u, cur.nsel);
-            t = 0;
-        } else {
+        if (!last_tile) {
             ++t;
+            continue;
         }
+        // 6. the unit is done: hand its per-head sums (reduced over this
+        //    warp's 32 key lanes) and its maxima to the output warps
+        if (nu > 0 && !mbar_wait(smem_addr(&ms.l_free), (nu - 1) & 1, ab, p.err)) return;
+        ms.red_l[c.qd][32 * c.hf + c.lane] = warp_transpose_reduce32<false>(lacc, c.lane);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lacc[h] = 0.0f;
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(smem_addr(&ms.l_ready));
+        ++nu;
+        if (!more) break;
+        u = u_next;
+        t = 0;
+    }
+}
+
+// ------------------------------------------------------------ output warps
+// One warp per TMEM lane quadrant, running beside the workers' next unit:
+// per-head factors of a finished unit (sink fold, or the partial's m and l),
+// then O^T read back 16 heads at a time, scaled and stored.  The stores take
+// about 4k cycles per unit (the SM writes ~32 bytes a clock); overlapped
+// with the next unit's gather, scores and softmax they leave its chain.
+__device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, int lane) {
+    volatile int* ab = &ms.abort_flag;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    int nu = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+        if (!mbar_wait(smem_addr(&ms.l_ready), nu & 1, ab, p.err)) return;
+        float f[2];     // heads lane and lane + 32
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = lane + 32 * e;
+            const float l = (ms.red_l[0][h] + ms.red_l[1][h]) + (ms.red_l[2][h] + ms.red_l[3][h]);
+            const float m = ms.m_ref[h];
+            f[e] = 1.0f;
+            if (!p.partial) {
+                const float mu = m == -INFINITY ? 0.0f : m;
+                const float s2 = h < p.H ? __ldg(p.sink + h) * kLog2e : 0.0f;
+                const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
+                const float e1 = exp2f(mu - mstar);
+                const float e2 = exp2f(s2 - mstar);
+                f[e] = e1 / (l * e1 + e2);
+            } else if (qd == 0) {
+                float* ml = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD +
+                            static_cast<size_t>(u) * 2 * kHeadsPad;
+                ml[h] = m;
+                ml[kHeadsPad + h] = l;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ms.l_free));
+        if (!mbar_wait(smem_addr(&ms.o_full), nu & 1, ab, p.err)) return;
+        tc_fence_after();
+        float* dst = p.partial ? p.part + static_cast<size_t>(u) * kHeadsPad * kD
+                               : p.out + static_cast<size_t>(u / p.chunks) * p.H * kD;
+        const int d0 = 32 * qd + lane;
+#pragma unroll 1
+        for (int hg = 0; hg < 4; ++hg) {
+            float fh[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) fh[j] = __shfl_sync(0xffffffffu, hg < 2 ? f[0] : f[1], 16 * (hg & 1) + j);
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                // chunks 0-2 keep the hi and lo halves 64 columns apart
+                const uint32_t ta = tmem + lane_off + tmem_o(i) + 16 * hg;
+                float o[16];
+                tmem_ld16(ta, o);
+                if (i < 3) {
+                    float lo[16];
+                    tmem_ld16(ta + 64, lo);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] += lo[j];
+                }
+                const int d = i * 128 + d0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int h = 16 * hg + j;
+                    if (h < p.H) dst[static_cast<size_t>(h) * kD + d] = o[j] * fh[j];
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ms.o_free));
     }
 }
 
@@ -577,17 +683,24 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
         return;
     }
     if (threadIdx.x == 0) {
-        mbar_init(smem_addr(&ms.kv_full), kWorkers);
-        mbar_init(smem_addr(&ms.kv_free), 1);
+        mbar_init(smem_addr(&ms.kv_full), 4 * kWorkers);   // one arrive per quarter tile and thread
+        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&ms.kv_free[i]), 1);
         mbar_init(smem_addr(&ms.s_full), 1);
-        mbar_init(smem_addr(&ms.p_full), kWorkers);
+        mbar_init(smem_addr(&ms.p_full), kWorkerWarps);
         mbar_init(smem_addr(&ms.q_full), 1);
         mbar_init(smem_addr(&ms.q_free), 1);
-        for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&ms.grp[i]), kWorkers);
+        mbar_init(smem_addr(&ms.p_ack), 1);
+        mbar_init(smem_addr(&ms.red_sync), kWorkerWarps);
+        for (int w = 0; w < kWorkerWarps; ++w) ms.ovf[w] = 0;
+        ms.redo = 0;
         mbar_init(smem_addr(&ms.drain), 1);
+        mbar_init(smem_addr(&ms.idx_full), 32);
+        mbar_init(smem_addr(&ms.o_full), 1);
+        mbar_init(smem_addr(&ms.o_free), kOutWarps);
+        mbar_init(smem_addr(&ms.l_ready), kWorkerWarps);
+        mbar_init(smem_addr(&ms.l_free), kOutWarps);
         for (int h = 0; h < 64; ++h) ms.m_ref[h] = -INFINITY;
         ms.abort_flag = 0;
-        ms.rescale_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&p.tmap_q);
     }
@@ -610,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
     const uint32_t tmem = ms.tmem_base;
 
     if (warp < kWorkerWarps) {
+        regs_inc<kRegsWorker>();
         int q_armed = 0;
         worker_role(p, smem, ms, tmem, q_armed);
         cp_async_wait_all();
@@ -619,8 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
             mbar_wait(smem_addr(&ms.q_full), (q_armed - 1) & 1, &dummy, p.err);
         }
         __syncwarp();
+    } else if (warp < kOutWarp0 + kOutWarps) {
+        regs_dec<kRegsOther>();
+        output_role(p, ms, tmem, warp & 3, threadIdx.x & 31);
+        __syncwarp();
     } else {
-        if ((threadIdx.x & 31) == 0) {
+        regs_dec<kRegsOther>();
+        if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
             mma_role(p, smem, ms, tmem);
             // every MMA this thread issued has completed before TMEM is freed
             umma_commit(smem_addr(&ms.drain));
