@@ -281,6 +281,13 @@ __device__ __forceinline__ float warp_max_f32(float v) {
     return r;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (a no-op for a launch without
+// the programmatic attribute), and let the grid launched after this one in
+// the stream start its own prologue.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // Warpgroup register reallocation (all 128 threads of the warpgroup execute it).
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_inc() {

@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
 // partial holds (m, l, O) with O and l relative to 2^m (2^0 when m is -inf,
 // in which case O and l are 0 or NaN).
 __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p) {
+    grid_launch_dependents();
+    grid_dependency_wait();          // the split kernel's partials are complete
     const int r = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x;
     const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
@@ -162,9 +164,18 @@ cudaError_t launch_simt(const SimtParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-    dim3 grid(p.R, p.H);
-    dsa_combine_kernel<<<grid, 128, 0, s>>>(p);
-    return cudaGetLastError();
+    // launched while the split kernel still runs; it waits for that kernel
+    // before it reads the partials
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.R), static_cast<unsigned>(p.H));
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dsa_combine_kernel, p);
 }
 
 }  // namespace dsa

@@ -678,7 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem[];
     Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
     const int warp = threadIdx.x >> 5;
+    grid_launch_dependents();        // the next grid in the stream may start its prologue
     if (smem_addr(smem) & 1023u) {   // the swizzle needs 1024-byte alignment
+        grid_dependency_wait();
         if (threadIdx.x == 0) atomicOr(p.err, DSA_DEVERR_LAYOUT);
         return;
     }
@@ -717,6 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
         }
         fence_proxy_async();
     }
+    // everything above touched only shared memory and TMEM; the inputs and
+    // outputs may belong to the grid before this one in the stream
+    grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -809,8 +814,20 @@ cudaError_t launch_tc(const TcParams& params, int grid, cudaStream_t s) {
     TcParams p = params;
     if (!encode_rows(&p.tmap_q, p.q, static_cast<uint64_t>(p.R) * p.H, static_cast<uint32_t>(p.H)))
         return cudaErrorInvalidValue;
-    dsa_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    // programmatic serialisation: the kernel's prologue may overlap the tail
+    // of the previous grid in the stream; it waits for that grid before it
+    // reads or writes global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dsa_tc_kernel, p);
 }
 
 }  // namespace dsa
