@@ -29,6 +29,8 @@
 //     sums and O^T rescaled).  Weights are written as two bf16 terms
 //     (P = hi + lo) so the value sum keeps ~14 bits; each thread keeps its
 //     key lane's running sums, reduced over the 128 lanes once per unit.
+//   * warp 13 (one thread) loads each unit's Q by TMA once the last score
+//     MMA of the unit before has read the buffer.
 //   * MMA warp 12 (one thread) issues tcgen05.mma:
 //       S^T[key][head]  = KV_tile (K-major, M=128) x Q^T (K-major, N=64)
 //       O^T[col][head] += V^T (MN-major, M=128 per 128 columns) x P^T
@@ -67,6 +69,7 @@ constexpr int kOutWarps = 4;
 constexpr int kMmaWarp = 12;
 constexpr int kThreads = 512;
 constexpr int kIdxWarp = kWorkerWarps - 1;   // copies each tile's indices ahead
+constexpr int kQWarp = kMmaWarp + 1;         // loads each unit's Q
 constexpr uint32_t kRegsWorker = 184;
 constexpr uint32_t kRegsOther = 72;
 // two warpgroups at kRegsWorker and two at kRegsOther use exactly the
@@ -95,8 +98,8 @@ __host__ __device__ constexpr uint32_t tmem_o(int i) { return 64u + 128u * stati
 
 struct Misc {
     uint64_t kv_full;       // workers' cp.async -> MMA: the KV tile landed
-    uint64_t kv_free[4];    // MMA -> workers: P.V is done with keys [0, 32(i+1)) of the
-                            // tile; [3]: with the whole buffer and O^T
+    uint64_t kv_free[5];    // MMA -> workers: P.V is done with keys [0, 32(i+1)) of the
+                            // tile for i < 3, [0, 112) for [3], all of them for [4]
     uint64_t s_full;        // MMA -> workers: scores of the tile ready
     uint64_t p_full;        // worker warps -> MMA: P written (and O^T rescaled)
     uint64_t q_full;        // Q TMA -> MMA: Q of the unit landed
@@ -272,12 +275,15 @@ __device__ __forceinline__ void pv_kstep(uint32_t tmem, uint64_t dV, uint64_t dP
 
 // Keys [32q, 32q + 32) of the tile, then a commit that frees those rows of
 // the KV buffer for the next tile's gather.
+// The last quarter is released in two halves, so only 16 rows are left to
+// gather once the P.V is over.
 template <int q>
 __device__ __forceinline__ void pv_quarter(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi,
                                            uint64_t dPlo, uint32_t acc0, Misc& ms) {
     pv_kstep<2 * q>(tmem, dV, dPst, dPhi, dPlo, acc0);
+    if (q == 3) umma_commit(smem_addr(&ms.kv_free[3]));
     pv_kstep<2 * q + 1>(tmem, dV, dPst, dPhi, dPlo, acc0);
-    umma_commit(smem_addr(&ms.kv_free[q]));
+    umma_commit(smem_addr(&ms.kv_free[q == 3 ? 4 : q]));
 }
 
 __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem) {
@@ -513,7 +519,7 @@ __device__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerC
     return true;
 }
 
-__device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem, int& q_armed) {
+__device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem) {
     WorkerCtx c;
     c.wt = threadIdx.x;
     c.w = c.wt >> 5;
@@ -525,20 +531,10 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
     c.ph_red = c.ph_ack = 0u;
     volatile int* ab = &ms.abort_flag;
     const uint32_t sKv = smem_addr(smem + kOffKv);
-    const uint32_t sQ = smem_addr(smem + kOffQ);
-    const uint32_t q_bytes = 8u * static_cast<uint32_t>(p.H) * 128u;
-    const bool q_thread = c.wt == 0;
 
     int u = blockIdx.x;
     if (u >= p.units) return;
     if (c.w == kIdxWarp) prefetch_idx(p, u, 0, ms, c.lane);
-    if (q_thread) {
-        const uint32_t bar = smem_addr(&ms.q_full);
-        mbar_arrive_expect_tx(bar, q_bytes);
-        for (int s = 0; s < 8; ++s)
-            tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u / p.chunks) * p.H, bar);
-        ++q_armed;
-    }
     Unit un;
     float lacc[32];
 #pragma unroll
@@ -560,7 +556,8 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[2]), ph, ab, p.err)) return;
         issue_rows<2>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
-        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[3]), ph, ab, p.err)) return;
+        // rows 96-111 (warps 0-3) are free one k-step before rows 112-127
+        if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[c.w < 4 ? 3 : 4]), ph, ab, p.err)) return;
         issue_rows<3>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
         const bool last_tile = t + 1 == un.tiles;
@@ -573,15 +570,6 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         //    (every thread has issued this tile's gather: idx[] is free)
         if (more && c.w == kIdxWarp) prefetch_idx(p, u_next, last_tile ? 0 : t + 1, ms, c.lane);
         // 5. weights
-        if (last_tile && more && q_thread) {
-            // the unit's last score MMA has read Q: load the next unit's
-            if (!mbar_wait(smem_addr(&ms.q_free), nu & 1, ab, p.err)) return;
-            const uint32_t bar = smem_addr(&ms.q_full);
-            mbar_arrive_expect_tx(bar, q_bytes);
-            for (int s = 0; s < 8; ++s)
-                tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u_next / p.chunks) * p.H, bar);
-            ++q_armed;
-        }
         if (!softmax_tile(p, smem, ms, c, tmem, un, t, nu, lacc)) return;
         ++g;
         if (!last_tile) {
@@ -600,6 +588,28 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         if (!more) break;
         u = u_next;
         t = 0;
+    }
+}
+
+// ------------------------------------------------------------------ Q load
+// One thread of a spare warp: loads each unit's Q by tiled TMA as soon as
+// the last score MMA of the unit before has read the buffer, off the
+// workers' path.
+__device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
+    volatile int* ab = &ms.abort_flag;
+    const uint32_t sQ = smem_addr(smem + kOffQ);
+    const uint32_t q_bytes = 8u * static_cast<uint32_t>(p.H) * 128u;
+    const uint32_t bar = smem_addr(&ms.q_full);
+    int nu = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+        if (nu > 0 && !mbar_wait(smem_addr(&ms.q_free), (nu - 1) & 1, ab, p.err)) break;
+        mbar_arrive_expect_tx(bar, q_bytes);
+        for (int s = 0; s < 8; ++s) tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u / p.chunks) * p.H, bar);
+    }
+    if (nu > 0) {
+        // the copies armed here have landed before the CTA can exit
+        int dummy = 0;
+        mbar_wait(bar, (nu - 1) & 1, &dummy, p.err);
     }
 }
 
@@ -686,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
     }
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&ms.kv_full), 4 * kWorkers);   // one arrive per quarter tile and thread
-        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&ms.kv_free[i]), 1);
+        for (int i = 0; i < 5; ++i) mbar_init(smem_addr(&ms.kv_free[i]), 1);
         mbar_init(smem_addr(&ms.s_full), 1);
         mbar_init(smem_addr(&ms.p_full), kWorkerWarps);
         mbar_init(smem_addr(&ms.q_full), 1);
@@ -729,14 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
 
     if (warp < kWorkerWarps) {
         regs_inc<kRegsWorker>();
-        int q_armed = 0;
-        worker_role(p, smem, ms, tmem, q_armed);
+        worker_role(p, smem, ms, tmem);
         cp_async_wait_all();
-        if (q_armed > 0) {
-            // the Q copies this thread armed have landed before the CTA can exit
-            int dummy = 0;
-            mbar_wait(smem_addr(&ms.q_full), (q_armed - 1) & 1, &dummy, p.err);
-        }
         __syncwarp();
     } else if (warp < kOutWarp0 + kOutWarps) {
         regs_dec<kRegsOther>();
@@ -744,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
         __syncwarp();
     } else {
         regs_dec<kRegsOther>();
+        if (warp == kQWarp && (threadIdx.x & 31) == 0) q_role(p, smem, ms);
         if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
             mma_role(p, smem, ms, tmem);
             // every MMA this thread issued has completed before TMEM is freed
