@@ -18,7 +18,8 @@
 //     128-byte-swizzled tile of 8 segments x 128 keys x 64 columns, 32 keys
 //     at a time as the previous tile's P.V releases them.  The tile is read
 //     once from global memory and serves every head, as keys and as values.
-//     The tile's indices arrive one tile ahead by cp.async, Q by tiled TMA.
+//     The tile's indices arrive one tile ahead by cp.async (warp 14), Q by
+//     tiled TMA (warp 13).
 //     Keys past n_sel are zero-filled; an out-of-range selection gathers a
 //     NaN row.
 //     softmax: worker w reads TMEM lane quadrant w%4 (32 keys) and heads
@@ -68,8 +69,8 @@ constexpr int kOutWarp0 = 8;
 constexpr int kOutWarps = 4;
 constexpr int kMmaWarp = 12;
 constexpr int kThreads = 512;
-constexpr int kIdxWarp = kWorkerWarps - 1;   // copies each tile's indices ahead
 constexpr int kQWarp = kMmaWarp + 1;         // loads each unit's Q
+constexpr int kIdxWarp = kMmaWarp + 2;       // copies each tile's indices ahead
 constexpr uint32_t kRegsWorker = 184;
 constexpr uint32_t kRegsOther = 72;
 // two warpgroups at kRegsWorker and two at kRegsOther use exactly the
@@ -534,7 +535,6 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
 
     int u = blockIdx.x;
     if (u >= p.units) return;
-    if (c.w == kIdxWarp) prefetch_idx(p, u, 0, ms, c.lane);
     Unit un;
     float lacc[32];
 #pragma unroll
@@ -566,17 +566,14 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         // 3. scores of this tile
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) return;
         tc_fence_after();
-        // 4. indices of the next tile, copied while the weights are computed
-        //    (every thread has issued this tile's gather: idx[] is free)
-        if (more && c.w == kIdxWarp) prefetch_idx(p, u_next, last_tile ? 0 : t + 1, ms, c.lane);
-        // 5. weights
+        // 4. weights
         if (!softmax_tile(p, smem, ms, c, tmem, un, t, nu, lacc)) return;
         ++g;
         if (!last_tile) {
             ++t;
             continue;
         }
-        // 6. the unit is done: hand its per-head sums (reduced over this
+        // 5. the unit is done: hand its per-head sums (reduced over this
         //    warp's 32 key lanes) and its maxima to the output warps
         if (nu > 0 && !mbar_wait(smem_addr(&ms.l_free), (nu - 1) & 1, ab, p.err)) return;
         ms.red_l[c.qd][32 * c.hf + c.lane] = warp_transpose_reduce32<false>(lacc, c.lane);
@@ -589,6 +586,36 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         u = u_next;
         t = 0;
     }
+}
+
+// ----------------------------------------------------------- index warp
+// A spare warp walks the same tiles as the workers and copies the indices of
+// tile g + 1 as soon as the scores of tile g are ready (by then every worker
+// has issued tile g's gather, so idx[] is free).
+__device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
+    volatile int* ab = &ms.abort_flag;
+    int u = blockIdx.x;
+    if (u >= p.units) return;
+    prefetch_idx(p, u, 0, ms, lane);
+    Unit un = unit_info(p, u);
+    int t = 0, g = 0;
+    while (true) {
+        int u2 = u, t2 = t + 1;
+        if (t2 == un.tiles) {
+            u2 = u + static_cast<int>(gridDim.x);
+            t2 = 0;
+        }
+        if (u2 >= p.units) break;
+        if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) break;
+        prefetch_idx(p, u2, t2, ms, lane);
+        if (u2 != u) {
+            u = u2;
+            un = unit_info(p, u);
+        }
+        t = t2;
+        ++g;
+    }
+    cp_async_wait_all();    // its copies land before the CTA can exit
 }
 
 // ------------------------------------------------------------------ Q load
@@ -749,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
     } else {
         regs_dec<kRegsOther>();
         if (warp == kQWarp && (threadIdx.x & 31) == 0) q_role(p, smem, ms);
+        if (warp == kIdxWarp) idx_role(p, ms, threadIdx.x & 31);
         if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
             mma_role(p, smem, ms, tmem);
             // every MMA this thread issued has completed before TMEM is freed
