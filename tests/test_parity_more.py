@@ -1,0 +1,101 @@
+"""More GPU parity: launch shapes the main parity file does not reach.
+
+- decode batches with more work units than SMs, so a CTA runs several units
+  and the combine merges chunk partials written in different rounds;
+- decode rows longer than 1024 keys (16 key chunks a row);
+- prefill rows whose unit count is not a multiple of the SM count;
+- the same calls captured into a CUDA graph, and issued on a side stream,
+  must give the same bits as direct calls on the current stream.
+
+Tolerances as in test_parity.py: bf16 |g-o| <= 3e-3 * max|o| over the
+(row, head), nonfinite classes exact.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from deepseek_v4_top_gb300 import inputs as I
+
+from gpu_helpers import compare, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    import torch
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+
+
+def _check(case):
+    got, code = run(case)
+    assert code == 0, "device error word %#x" % code
+    ref, _ = oracle.attn(case)
+    return compare(case, got, ref)
+
+
+def test_decode_more_units_than_sms():
+    # 48 rows x 5 chunks = 240 units on at most 152 SMs
+    rng = np.random.default_rng(4101)
+    _check(I._edge_base(rng, "decode_b48", I.BF16, 64, 640, "decode", R=48, N=2048, k_extra=0))
+
+
+@pytest.mark.parametrize("k", [1024, 1025, 2048])
+def test_decode_long_rows(k):
+    # 8, 9 and 16 key chunks a row, rows ragged below k
+    rng = np.random.default_rng(4200 + k)
+    _check(I._edge_base(rng, "decode_k%d" % k, I.BF16, 64, k, "decode", R=3, N=4096, k_extra=1))
+
+
+def test_prefill_rows_not_a_multiple_of_the_grid():
+    # 157 rows: the last round of the persistent grid is 5 rows
+    rng = np.random.default_rng(4300)
+    _check(I._edge_base(rng, "prefill_r157", I.BF16, 64, 640, "prefill", R=157, N=1024, k_extra=0))
+
+
+def _calls(d, case, out, stream):
+    from deepseek_v4_top_gb300 import dsa
+    fn = dsa.dsa_sparse_attn_decode if case.mode == "decode" else dsa.dsa_sparse_attn_prefill
+    fn(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], case.scale, out, stream)
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_graph_replay_and_side_stream_match_direct_calls(mode):
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    rng = np.random.default_rng(4400)
+    case = I._edge_base(rng, "graph_" + mode, I.BF16, 64, 300, mode, R=6, N=2048, k_extra=2)
+    d = to_device(case)
+    shape = (case.R, case.H, 512)
+    direct = torch.empty(shape, dtype=torch.float32, device="cuda")
+    _calls(d, case, direct, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    on_side = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(side):
+        _calls(d, case, on_side, side)
+    side.synchronize()
+
+    replayed = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            _calls(d, case, replayed, torch.cuda.current_stream())
+        replayed.fill_(float("nan"))
+        g.replay()
+        g.replay()
+    side.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+
+    a = direct.cpu().numpy().view(np.uint32)
+    assert np.array_equal(a, on_side.cpu().numpy().view(np.uint32))
+    assert np.array_equal(a, replayed.cpu().numpy().view(np.uint32))
+    ref, _ = oracle.attn(case)
+    compare(case, direct.cpu().numpy(), ref)
