@@ -104,7 +104,7 @@ struct Misc {
     uint64_t s_full;        // MMA -> workers: scores of the tile ready
     uint64_t p_full;        // worker warps -> MMA: P written (and O^T rescaled)
     uint64_t q_full;        // Q TMA -> MMA: Q of the unit landed
-    uint64_t q_free;        // MMA -> worker 0: last score MMA of the unit done
+    uint64_t q_free;        // MMA -> Q warp: last score MMA of the unit done (Q may be reloaded)
     uint64_t p_ack;         // MMA -> workers: P accepted, or ms.redo set
     uint64_t red_sync;      // worker-warp sync of the tile-maxima reduction (one arrival per warp)
     uint64_t drain;         // MMA thread: everything it issued completed

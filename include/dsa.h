@@ -37,7 +37,13 @@
  *   buffer for split partial results are allocated once per device on first
  *   use (the scratch grows when a larger batch needs it) and released by
  *   dsa_shutdown().  Do not issue the first call of a device inside a CUDA
- *   graph capture.
+ *   graph capture.  Decode calls whose work overlaps on the GPU (other
+ *   streams, other threads) share that scratch and race; order them on one
+ *   stream.
+ * - The kernels are launched with programmatic stream serialisation: a
+ *   kernel may start its set-up while the previous work on the stream is
+ *   finishing, but it touches no global memory before that work has
+ *   completed, so stream order holds as for an ordinary launch.
  * - Host-side errors return before anything is launched.
  * - Device-side errors: an index in idx[r][0..n_sel[r]) outside [0, N), or an
  *   n_sel[r] outside [0, k_max], sets a bit in a sticky device error word and
