@@ -88,6 +88,9 @@ def test_rescaling_when_later_tiles_score_higher(mode):
     """Block maxima climbing by ~5.7 per 128 keys force the running reference
     maximum to move, so the accumulated value sum and row sum are rescaled."""
     _check_full(I.rising_scores(mode=mode))
+    # blocks that climb by ~41 log2 units each: every later tile passes the
+    # lag the kernel allows its reference maxima, so every one rescales
+    _check_full(I.rising_scores(mode=mode, step=160.0))
 
 
 @pytest.mark.parametrize("mode", ["decode", "prefill"])
