@@ -122,29 +122,51 @@ __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p)
     const int r = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x;
     const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
+    const size_t u0 = static_cast<size_t>(r) * p.chunks;
+    // Chunks are taken kBatch at a time, all loads of a batch issued before
+    // any of them is used; the arithmetic runs in chunk order.
+    constexpr int kBatch = 8;
     float M = -INFINITY;
     bool have = false;
-    for (int c = 0; c < p.chunks; ++c) {
-        const float mc = ml_base[(static_cast<size_t>(r) * p.chunks + c) * 2 * kHeadsPad + h];
-        if (mc != -INFINITY) {
-            M = have ? fmaxf(M, mc) : mc;
-            have = true;
+    for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
+        float mv[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            mv[j] = c0 + j < p.chunks ? ml_base[(u0 + c0 + j) * 2 * kHeadsPad + h] : -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (mv[j] != -INFINITY) {
+                M = have ? fmaxf(M, mv[j]) : mv[j];
+                have = true;
+            }
         }
     }
     const float mu = have ? M : 0.0f;
     float l = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < p.chunks; ++c) {
-        const size_t u = static_cast<size_t>(r) * p.chunks + c;
-        const float mc = ml_base[u * 2 * kHeadsPad + h];
-        const float lc = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
-        const float w = (mc == -INFINITY) ? 1.0f : exp2f(mc - mu);
-        l += w * lc;
-        const float4 o = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+    for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
+        float mv[kBatch], lv[kBatch];
+        float4 ov[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (c0 + j < p.chunks) {
+                const size_t u = u0 + c0 + j;
+                mv[j] = ml_base[u * 2 * kHeadsPad + h];
+                lv[j] = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
+                ov[j] = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (c0 + j < p.chunks) {
+                const float w = (mv[j] == -INFINITY) ? 1.0f : exp2f(mv[j] - mu);
+                l += w * lv[j];
+                acc.x = fmaf(w, ov[j].x, acc.x);
+                acc.y = fmaf(w, ov[j].y, acc.y);
+                acc.z = fmaf(w, ov[j].z, acc.z);
+                acc.w = fmaf(w, ov[j].w, acc.w);
+            }
+        }
     }
     const float s2 = p.sink[h] * kLog2e;
     const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
