@@ -52,9 +52,14 @@ dsa_status device_state(DeviceState** out) {
     return DSA_OK;
 }
 
-dsa_status ensure_scratch(DeviceState* st, size_t bytes) {
+// Grows the decode scratch to `bytes` and returns it (under the lock, so a
+// concurrent grow cannot free it between the check and the use).
+dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (st->scratch_bytes >= bytes) return DSA_OK;
+    if (st->scratch_bytes >= bytes) {
+        *out = st->scratch;
+        return DSA_OK;
+    }
     if (st->scratch) {
         // the old buffer may still be read by queued work
         if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
@@ -64,6 +69,7 @@ dsa_status ensure_scratch(DeviceState* st, size_t bytes) {
     }
     if (cudaMalloc(&st->scratch, bytes) != cudaSuccess) return DSA_ERR_CUDA;
     st->scratch_bytes = bytes;
+    *out = st->scratch;
     return DSA_OK;
 }
 
@@ -71,7 +77,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
                       const float* sink, const float* out, int R, int H, int N, int k_max,
-                      dsa_dtype dtype) {
+                      dsa_dtype dtype, bool decode) {
     if (R < 0 || N <= 0 || k_max <= 0 || H <= 0) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
     if (H > kHeadsPad) return DSA_ERR_UNSUPPORTED;   // heads are padded to 64 on chip
@@ -82,8 +88,8 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
     if (static_cast<long long>(R) * ((k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys) > (1LL << 30))
         return DSA_ERR_INVALID_ARG;
     if (dtype == DSA_F32 && R > 65535) return DSA_ERR_UNSUPPORTED;
-    // the tensor-core kernel addresses cache rows and q rows with int32
-    if (static_cast<long long>(R) * N >= (1LL << 31) || static_cast<long long>(R) * H >= (1LL << 31))
+    // the kernels index q rows, and a decode batch's cache rows, with int32
+    if ((decode && static_cast<long long>(R) * N >= (1LL << 31)) || static_cast<long long>(R) * H >= (1LL << 31))
         return DSA_ERR_INVALID_ARG;
     return DSA_OK;
 }
@@ -91,7 +97,7 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
 dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
                const float* sink, float scale, float* out, int R, int H, int N, int k_max,
                dsa_dtype dtype, void* stream, bool decode) {
-    dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype);
+    dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype, decode);
     if (st != DSA_OK || R == 0) return st;
     DeviceState* ds = nullptr;
     st = device_state(&ds);
@@ -139,9 +145,8 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     if (p.partial) {
         const size_t bytes =
             static_cast<size_t>(p.units) * kPartialFloats * sizeof(float);
-        st = ensure_scratch(ds, bytes);
+        st = ensure_scratch(ds, bytes, &p.part);
         if (st != DSA_OK) return st;
-        p.part = ds->scratch;
     }
     const int grid = p.units < ds->sm_count ? p.units : ds->sm_count;
     if (launch_tc(p, grid, s) != cudaSuccess) return DSA_ERR_CUDA;

@@ -50,6 +50,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -801,9 +803,12 @@ size_t tc_smem_bytes() { return kSmemBytes; }
 
 namespace {
 
+std::mutex g_launch_mu;    // guards the one-time set-up below
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
+    std::lock_guard<std::mutex> lock(g_launch_mu);
     if (!tried) {
         tried = true;
         void* f = nullptr;
@@ -838,11 +843,15 @@ cudaError_t launch_tc(const TcParams& params, int grid, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(dsa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_launch_mu);
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(dsa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes));
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
     }
     TcParams p = params;
     if (!encode_rows(&p.tmap_q, p.q, static_cast<uint64_t>(p.R) * p.H, static_cast<uint32_t>(p.H)))
