@@ -107,10 +107,10 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22; 2^-inf = 0,
-// NaN stays NaN).
-__device__ __forceinline__ float ex2_approx(float x) {
+// NaN stays NaN).  Results below 2^-126 flush to zero.
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 

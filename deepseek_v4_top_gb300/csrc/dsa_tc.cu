@@ -12,7 +12,7 @@
 // shared-memory KV tile (128 KiB) is busy from its gather to the end of its
 // P.V.  Sixteen warps in four warpgroups:
 //
-//   * worker warps 0-7 (184 registers each, by setmaxnreg):
+//   * worker warps 0-7 (176 registers each, by setmaxnreg):
 //     gather: 16-byte cp.async of whole 1 KiB rows (each thread copies 16
 //     bytes of each 128-byte column segment, back to back) straight into a
 //     128-byte-swizzled tile of 8 segments x 128 keys x 64 columns, 32 keys
@@ -64,7 +64,7 @@ namespace {
 
 // Four warpgroups: two of worker warps, one of output warps (one per TMEM
 // lane quadrant), one holding the MMA warp.  The launch gives every thread
-// 128 registers; the workers take 184 and the others keep 72.
+// 128 registers; the workers take 176 and the others keep 80.
 constexpr int kWorkerWarps = 8;
 constexpr int kWorkers = 32 * kWorkerWarps;
 constexpr int kOutWarp0 = 8;
@@ -73,8 +73,8 @@ constexpr int kMmaWarp = 12;
 constexpr int kThreads = 512;
 constexpr int kQWarp = kMmaWarp + 1;         // loads each unit's Q
 constexpr int kIdxWarp = kMmaWarp + 2;       // copies each tile's indices ahead
-constexpr uint32_t kRegsWorker = 184;
-constexpr uint32_t kRegsOther = 72;
+constexpr uint32_t kRegsWorker = 176;
+constexpr uint32_t kRegsOther = 80;
 // two warpgroups at kRegsWorker and two at kRegsOther use exactly the
 // 65536 registers that 512 threads x 128 bring
 static_assert((2 * kRegsWorker + 2 * kRegsOther) * 128 == 65536 && 65536 / kThreads == 128,
@@ -437,17 +437,47 @@ __device__ bool new_reference(const TcParams& p, Misc& ms, WorkerCtx& c, uint32_
     return true;
 }
 
-// Weights relative to the references (0 when a reference is -inf) replace
-// the scores in x and are written to P as two bf16 terms: hi is the top 16
-// bits of the fp32 weight, lo the top 16 bits of the exact remainder, so
-// hi + lo is within 2^-14 of the weight (relative) and the split takes no
-// conversion instructions.  This key's row, this thread's 4 chunks of 8 heads.
-__device__ __forceinline__ void write_p(uint8_t* smem, const WorkerCtx& c, float* x, const float* mref) {
+// Weights of this thread's key for its 32 heads, in place over the raw
+// scores in x: 2^(s*sc - m_h), one FFMA and one ex2 each (the reference's
+// negation is an operand modifier); 0 for a key past n_valid.  A head whose
+// reference is still -inf (no finite score yet) weighs against 0 instead,
+// on a separate path that the warp takes as a whole (its lanes share their
+// heads).  Returns whether a valid score passes its reference by more than
+// 2^kTau.
+__device__ __forceinline__ bool tile_weights(float* x, bool valid, float sc, const float* mref, bool ninf) {
+    bool ovf = false;
+    if (!ninf) {
 #pragma unroll
-    for (int h = 0; h < 32; ++h) {
-        const float mu = mref[h] == -INFINITY ? 0.0f : mref[h];
-        x[h] = ex2_approx(x[h] - mu);
+        for (int h = 0; h < 32; ++h) {
+            const float d = fmaf(x[h], sc, -mref[h]);
+            ovf |= d > kTau;
+            x[h] = valid ? ex2_approx_ftz(d) : 0.0f;
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            const float s = x[h] * sc;
+            ovf |= s > mref[h] + kTau;
+            const float mu = mref[h] == -INFINITY ? 0.0f : mref[h];
+            x[h] = valid ? ex2_approx_ftz(s - mu) : 0.0f;
+        }
     }
+    return valid && ovf;
+}
+
+// Whether any of this thread's 32 references is -inf.
+__device__ __forceinline__ bool any_ninf(const float* mref) {
+    bool any = false;
+#pragma unroll
+    for (int h = 0; h < 32; ++h) any |= mref[h] == -INFINITY;
+    return any;
+}
+
+// Writes the weights in x to P as two bf16 terms: hi is the top 16 bits of
+// the fp32 weight, lo the top 16 bits of the exact remainder, so hi + lo is
+// within 2^-14 of the weight (relative) and the split takes no conversion
+// instructions.  This key's row, this thread's 4 chunks of 8 heads.
+__device__ __forceinline__ void store_p(uint8_t* smem, const WorkerCtx& c, const float* x) {
     uint8_t* prow_hi = smem + kOffPhi + c.key * 128;
     uint8_t* prow_lo = smem + kOffPlo + c.key * 128;
 #pragma unroll
@@ -480,41 +510,35 @@ __device__ __forceinline__ bool publish_p(const TcParams& p, Misc& ms, WorkerCtx
     return true;
 }
 
-// Softmax of one tile: weights into P, running sums into lacc.  Later tiles
-// use the current references optimistically; a warp that sees a score more
-// than 2^kTau above its reference flags the tile, and the MMA warp then has
-// every worker redo it with new references before any P.V reads P.
-__device__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerCtx& c, uint32_t tmem,
-                             const Unit& un, int t, int nu, float* lacc) {
+// Softmax of one tile: weights into P, running sums into lacc.  mref holds
+// this thread's references across tiles (ninf: one of them is -inf).  Later
+// tiles use them optimistically; a warp that sees a score more than 2^kTau
+// above its reference flags the tile, and the MMA warp then has every
+// worker redo it with new references before any P.V reads P.
+__device__ __forceinline__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerCtx& c, uint32_t tmem,
+                             const Unit& un, int t, int nu, float* lacc, float* mref, bool& ninf) {
     const uint32_t ts = tmem + c.lane_off + kTmemS + 32 * c.hf;
     const bool valid = t * 128 + c.key < un.n_valid;
-    float x[32], mref[32];
-    load_scores(ts, valid, p.scale_log2, x);
-    bool ovf = false;
+    float x[32];
     if (t == 0) {
-        if (!new_reference<true>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
         load_scores(ts, valid, p.scale_log2, x);
-    } else {
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(&ms.m_ref[32 * c.hf + 4 * h4]);
-            mref[4 * h4] = m4.x;
-            mref[4 * h4 + 1] = m4.y;
-            mref[4 * h4 + 2] = m4.z;
-            mref[4 * h4 + 3] = m4.w;
-        }
-#pragma unroll
-        for (int h = 0; h < 32; ++h) ovf |= x[h] > mref[h] + kTau;
-        ovf = __any_sync(0xffffffffu, ovf);
+        if (!new_reference<true>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
+        ninf = any_ninf(mref);
     }
-    write_p(smem, c, x, mref);
+    tmem_ld32(ts, x);
+    // the first tile's references are its maxima: nothing can pass them
+    bool ovf = tile_weights(x, valid, p.scale_log2, mref, ninf) && t > 0;
+    ovf = __any_sync(0xffffffffu, ovf);
+    store_p(smem, c, x);
     if (ovf && c.lane == 0) ms.ovf[c.w] = 1;
     if (!publish_p(p, ms, c)) return false;
     if (ms.redo) {
         load_scores(ts, valid, p.scale_log2, x);
         if (!new_reference<false>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
-        load_scores(ts, valid, p.scale_log2, x);
-        write_p(smem, c, x, mref);
+        ninf = any_ninf(mref);
+        tmem_ld32(ts, x);
+        tile_weights(x, valid, p.scale_log2, mref, ninf);
+        store_p(smem, c, x);
         if (!publish_p(p, ms, c)) return false;
     }
 #pragma unroll
@@ -538,7 +562,8 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
     int u = blockIdx.x;
     if (u >= p.units) return;
     Unit un;
-    float lacc[32];
+    float lacc[32], mref[32];   // this thread's running sums and references (set by each unit's first tile)
+    bool ninf = true;
 #pragma unroll
     for (int h = 0; h < 32; ++h) lacc[h] = 0.0f;
     int t = 0, g = 0, nu = 0;
@@ -569,7 +594,7 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) return;
         tc_fence_after();
         // 4. weights
-        if (!softmax_tile(p, smem, ms, c, tmem, un, t, nu, lacc)) return;
+        if (!softmax_tile(p, smem, ms, c, tmem, un, t, nu, lacc, mref, ninf)) return;
         ++g;
         if (!last_tile) {
             ++t;
