@@ -14,12 +14,17 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Prefill launches with more rows than CTAs hand rows out from a queue in
+// device memory (two ints); each stream gets its own, up to this many a device.
+constexpr int kQueues = 64;
 
 struct DeviceState {
-    uint32_t* err = nullptr;
+    uint32_t* err = nullptr;       // error word, followed by the stream queues
     float* scratch = nullptr;
     size_t scratch_bytes = 0;
     int sm_count = 0;
+    cudaStream_t queue_stream[kQueues] = {};
+    int queues_used = 0;
 };
 
 std::mutex g_mu;
@@ -40,8 +45,9 @@ dsa_status device_state(DeviceState** out) {
             return DSA_ERR_CUDA;
         if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED;   // built for sm_103a only
         uint32_t* e = nullptr;
-        if (cudaMalloc(&e, sizeof(uint32_t)) != cudaSuccess) return DSA_ERR_CUDA;
-        if (cudaMemset(e, 0, sizeof(uint32_t)) != cudaSuccess) {
+        const size_t bytes = (4 + 2 * kQueues) * sizeof(uint32_t);
+        if (cudaMalloc(&e, bytes) != cudaSuccess) return DSA_ERR_CUDA;
+        if (cudaMemset(e, 0, bytes) != cudaSuccess) {
             cudaFree(e);
             return DSA_ERR_CUDA;
         }
@@ -71,6 +77,27 @@ dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
     st->scratch_bytes = bytes;
     *out = st->scratch;
     return DSA_OK;
+}
+
+// The row queue of stream s, or null (round-robin rows) when s may run on
+// several threads' behalf at once (the per-thread default stream), while s
+// is being captured into a graph (a replay could overlap other work that
+// uses the same queue), or when every queue is taken.  Calls on one stream
+// run in order, so they never use a queue at the same time.
+int* stream_queue(DeviceState* st, cudaStream_t s) {
+    if (s == cudaStreamPerThread) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int slot = -1;
+    for (int i = 0; i < st->queues_used; ++i)
+        if (st->queue_stream[i] == s) slot = i;
+    if (slot < 0) {
+        if (st->queues_used == kQueues) return nullptr;
+        slot = st->queues_used++;
+        st->queue_stream[slot] = s;
+    }
+    return reinterpret_cast<int*>(st->err) + 4 + 2 * slot;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -131,6 +158,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     p.out = out;
     p.part = nullptr;
     p.err = ds->err;
+    p.queue = nullptr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.R = R;
     p.H = H;
@@ -149,6 +177,9 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
         if (st != DSA_OK) return st;
     }
     const int grid = p.units < ds->sm_count ? p.units : ds->sm_count;
+    // rows of unequal speed (SMs differ by a few percent) balance through a
+    // queue when there are more of them than CTAs
+    if (!p.partial && p.units > grid) p.queue = stream_queue(ds, s);
     if (launch_tc(p, grid, s) != cudaSuccess) return DSA_ERR_CUDA;
     if (p.partial) {
         CombineParams c;

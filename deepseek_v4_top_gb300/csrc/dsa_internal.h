@@ -31,6 +31,8 @@ struct TcParams {
     float* out;               // final mode: [R][H][512]
     float* part;              // partial mode: O [units][64][512] then (m, l) [units][2][64]
     uint32_t* err;            // device error word
+    int* queue;               // null: units round-robin over the grid; else the launch's unit
+                              // queue [next ticket, CTAs finished], zero at launch, left zero
     float scale_log2;         // scale * log2(e)
     int R, H, N, k_max;
     int decode;               // 1: row r reads slot r

@@ -106,6 +106,7 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
     p.out = out;
     p.part = d->base + kHeaderFloats;
     p.err = err;
+    p.queue = nullptr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.R = B;
     p.H = H;

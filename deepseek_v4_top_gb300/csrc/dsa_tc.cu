@@ -7,7 +7,10 @@
 // TensorFold PR #1206, "What changes": per-head sinks).
 //
 // How (one CTA per SM, persistent over work units; a unit is one row, or one
-// key chunk of a row when a decode batch is split across SMs).  Per 128-key
+// key chunk of a row when a decode batch is split across SMs).  A prefill
+// launch with more rows than CTAs hands rows out from a queue in device
+// memory (warp 14 takes them, one unit ahead), since SMs run at slightly
+// different speeds; otherwise units go round-robin over the grid.  Per 128-key
 // tile the work is a chain: gather -> scores -> softmax -> P.V, and the one
 // shared-memory KV tile (128 KiB) is busy from its gather to the end of its
 // P.V.  Sixteen warps in four warpgroups:
@@ -23,11 +26,14 @@
 //     Keys past n_sel are zero-filled; an out-of-range selection gathers a
 //     NaN row.
 //     softmax: worker w reads TMEM lane quadrant w%4 (32 keys) and heads
-//     32*(w/4) .. +31.  A unit's first tile sets per-head reference maxima
-//     (warp transpose reduction, one sync).  Later tiles use them
-//     optimistically; a score more than 2^8 above its reference flags the
-//     tile and the MMA warp has it redone with moved references (running
-//     sums and O^T rescaled).  Weights are written as two bf16 terms
+//     32*(w/4) .. +31.  With finite sinks a unit starts from per-head
+//     reference maxima equal to the sink logits; otherwise its first tile
+//     sets them to the tile's maxima (warp transpose reduction, one sync).
+//     The references are used optimistically: a score more than 2^32 above
+//     its reference, or a sink-seeded first tile that leaves a head without
+//     a weight of at least 2^-100, flags the tile and the MMA warp has it
+//     redone with moved references (running sums and O^T rescaled; a
+//     flagged first tile takes its exact maxima).  Weights are written as two bf16 terms
 //     (P = hi + lo) so the value sum keeps ~14 bits; each thread keeps its
 //     key lane's running sums, reduced over the 128 lanes once per unit.
 //   * warp 13 (one thread) loads each unit's Q by TMA once the last score
@@ -79,7 +85,13 @@ constexpr uint32_t kRegsOther = 80;
 // 65536 registers that 512 threads x 128 bring
 static_assert((2 * kRegsWorker + 2 * kRegsOther) * 128 == 65536 && 65536 / kThreads == 128,
               "the register split must add up to what the launch provides");
-constexpr float kTau = 8.0f;            // log2 units
+// A reference maximum may lag the scores by up to 2^kTau (log2 units): the
+// weights stay below 2^32 and a unit's sums below 2^42.
+constexpr float kTau = 32.0f;
+// A unit whose first tile is weighed against the sinks must give every head
+// with a selected key a weight of at least 2^kLowest (log2 units); else the
+// tile is redone with its exact maxima.
+constexpr float kLowest = -100.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kSegBytes = 128 * 128;          // 128 keys x 128 B
@@ -119,7 +131,11 @@ struct Misc {
     alignas(16) float red[4][64];       // [TMEM lane quadrant][head]: tile maxima
     alignas(16) float red_l[4][64];     // [TMEM lane quadrant][head]: a finished unit's sums
     alignas(16) float m_ref[64];        // per-head reference maximum (log2 units)
-    int ovf[kWorkerWarps];              // per worker warp: a score passed its reference max
+    uint64_t unit_full[4];  // index warp -> all roles: unit_ring[nu % 4] holds the CTA's nu-th unit
+    int unit_ring[4];       // units taken from the launch's queue, in the CTA's order
+    int ovf;                            // a worker warp saw a score pass its reference max
+    uint32_t seen[2];       // per head half, a unit's first tile weighed against the sinks: bit h
+                            // set if head 32*half+h has a weight >= 2^kLowest
     uint32_t tmem_base;
     int abort_flag;
     int redo;                           // the flagged tile is to be redone
@@ -145,6 +161,13 @@ struct Unit {
     int r, c, n_valid, tiles, bad_n;
 };
 
+// Whether every sink of the launch is finite (the same answer in every lane).
+__device__ __forceinline__ bool sinks_finite(const TcParams& p, int lane) {
+    const bool a = lane >= p.H || isfinite(__ldg(p.sink + lane));
+    const bool b = lane + 32 >= p.H || isfinite(__ldg(p.sink + lane + 32));
+    return __all_sync(0xffffffffu, a && b);
+}
+
 __device__ __forceinline__ Unit unit_from(const TcParams& p, int u, int ns) {
     Unit x;
     x.r = u / p.chunks;
@@ -160,6 +183,33 @@ __device__ __forceinline__ Unit unit_from(const TcParams& p, int u, int ns) {
 
 __device__ __forceinline__ Unit unit_info(const TcParams& p, int u) {
     return unit_from(p, u, __ldg(p.n_sel + u / p.chunks));
+}
+
+// The CTA's nu-th unit, or p.units when it has no more: round-robin over
+// the grid, or, with a launch queue (p.queue), the units the index warp has
+// taken from it in turn.  A row's result does not depend on which CTA runs it.
+__device__ __forceinline__ int unit_at(const TcParams& p, Misc& ms, int nu) {
+    if (!p.queue) return blockIdx.x + nu * static_cast<int>(gridDim.x);
+    if (!mbar_wait(smem_addr(&ms.unit_full[nu & 3]), (nu >> 2) & 1, &ms.abort_flag, p.err)) return p.units;
+    return *reinterpret_cast<volatile int*>(&ms.unit_ring[nu & 3]);
+}
+
+// Index warp: takes the next unit of the launch queue as the CTA's nu-th
+// and publishes it in the ring (p.units once the queue is empty).  It runs
+// one unit ahead of the CTA, and a unit's slot is reused four units later,
+// when every role has long read it: the slowest reader, the output warps,
+// read the CTA's unit nu - 2 before any P.V of unit nu - 1 can start (that
+// waits for them), and the ring is filled for unit nu + 1 only once the
+// scores of unit nu - 1's last tile are done.
+__device__ __forceinline__ int take_unit(const TcParams& p, Misc& ms, int nu, int lane) {
+    int u = 0;
+    if (lane == 0) {
+        const int ticket = atomicAdd(p.queue, 1);
+        u = ticket < p.units ? ticket : p.units;
+        ms.unit_ring[nu & 3] = u;
+        mbar_arrive(smem_addr(&ms.unit_full[nu & 3]));
+    }
+    return __shfl_sync(0xffffffffu, u, 0);
 }
 
 // Sync of the worker warps: one arrival per warp (after __syncwarp, which
@@ -289,7 +339,7 @@ __device__ __forceinline__ void pv_quarter(uint32_t tmem, uint64_t dV, uint64_t 
     umma_commit(smem_addr(&ms.kv_free[q == 3 ? 4 : q]));
 }
 
-__device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem) {
+__device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem, bool sinks) {
     const uint32_t sKv = smem_addr(smem + kOffKv);
     const uint32_t sQ = smem_addr(smem + kOffQ);
     const uint32_t sPhi = smem_addr(smem + kOffPhi);
@@ -304,7 +354,12 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
     const uint64_t dPlo = sdesc_sw128(sPlo, 1024, 1024);
     int g = 0, nu = 0;
     uint32_t ph_p = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+    // heads of the launch, per head half
+    const uint32_t need0 = p.H >= 32 ? 0xFFFFFFFFu : (1u << p.H) - 1u;
+    const uint32_t need1 = p.H >= 64 ? 0xFFFFFFFFu : (p.H > 32 ? (1u << (p.H - 32)) - 1u : 0u);
+    for (;; ++nu) {
+        const int u = unit_at(p, ms, nu);
+        if (u >= p.units) break;
         const Unit un = unit_info(p, u);
         if (!mbar_wait(smem_addr(&ms.q_full), nu & 1, ab, p.err)) return;
         for (int t = 0; t < un.tiles; ++t, ++g) {
@@ -320,13 +375,17 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
             if (!mbar_wait(smem_addr(&ms.p_full), ph_p, ab, p.err)) return;
             ph_p ^= 1u;
             // a tile that a worker warp flagged is redone with new reference maxima
-            volatile int* ovf = ms.ovf;
-            int flagged = 0;
-#pragma unroll
-            for (int w = 0; w < kWorkerWarps; ++w) flagged |= ovf[w];
+            volatile int* ovf = &ms.ovf;
+            int flagged = *ovf;
+            if (t == 0 && sinks) {
+                // a sink-seeded first tile must leave every head a weight >= 2^kLowest
+                volatile uint32_t* seen = ms.seen;
+                if (un.n_valid > 0 && ((seen[0] & need0) != need0 || (seen[1] & need1) != need1)) flagged = 1;
+                seen[0] = 0;
+                seen[1] = 0;
+            }
             if (flagged) {
-#pragma unroll
-                for (int w = 0; w < kWorkerWarps; ++w) ovf[w] = 0;
+                *ovf = 0;
                 *reinterpret_cast<volatile int*>(&ms.redo) = 1;
                 mbar_arrive(smem_addr(&ms.p_ack));
                 if (!mbar_wait(smem_addr(&ms.p_full), ph_p, ab, p.err)) return;
@@ -350,6 +409,7 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
 // ----------------------------------------------------------------- workers
 struct WorkerCtx {
     int wt, w, lane, qd, hf, key;   // thread, warp, lane, TMEM lane quadrant, head half, key in tile
+    bool sinks;                     // every sink is finite: units start from sink references
     uint32_t lane_off;
     uint32_t ph_red, ph_ack;        // phases of red_sync and p_ack
 };
@@ -444,9 +504,23 @@ __device__ bool new_reference(const TcParams& p, Misc& ms, WorkerCtx& c, uint32_
 // on a separate path that the warp takes as a whole (its lanes share their
 // heads).  Returns whether a valid score passes its reference by more than
 // 2^kTau.
-__device__ __forceinline__ bool tile_weights(float* x, bool valid, float sc, const float* mref, bool ninf) {
+template <bool kSeen = false>
+__device__ __forceinline__ bool tile_weights(float* x, bool valid, float sc, const float* mref, bool ninf,
+                                             uint32_t* seen = nullptr) {
     bool ovf = false;
-    if (!ninf) {
+    if (kSeen) {
+        // references from the sinks (all finite); bit h of *seen: this key
+        // gives head h a weight of at least 2^kLowest
+        uint32_t m = 0;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            const float d = fmaf(x[h], sc, -mref[h]);
+            ovf |= d > kTau;
+            m |= (d >= kLowest) ? (1u << h) : 0u;
+            x[h] = valid ? ex2_approx_ftz(d) : 0.0f;
+        }
+        *seen = valid ? m : 0u;
+    } else if (!ninf) {
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
             const float d = fmaf(x[h], sc, -mref[h]);
@@ -510,29 +584,67 @@ __device__ __forceinline__ bool publish_p(const TcParams& p, Misc& ms, WorkerCtx
     return true;
 }
 
+// Sink logit of head h in log2 units, the reference a unit's first tile
+// starts from when every sink is finite (0 for a padding head).
+__device__ __forceinline__ float sink_ref(const TcParams& p, int h) {
+    return h < p.H ? __ldg(p.sink + h) * kLog2e : 0.0f;
+}
+
 // Softmax of one tile: weights into P, running sums into lacc.  mref holds
-// this thread's references across tiles (ninf: one of them is -inf).  Later
-// tiles use them optimistically; a warp that sees a score more than 2^kTau
-// above its reference flags the tile, and the MMA warp then has every
-// worker redo it with new references before any P.V reads P.
+// this thread's references across tiles (ninf: one of them is -inf).
+// With finite sinks (c.sinks) a unit starts from references equal to the
+// sink logits, loaded into mref during the gather; otherwise its first tile
+// sets them to the tile's exact maxima (a reduction over the worker warps).
+// The references are used optimistically: a warp that sees a score more
+// than 2^kTau above its reference flags the tile (and so does the MMA warp
+// when a sink-seeded first tile leaves a head without a weight of at least
+// 2^kLowest); every worker then redoes the tile with new references before
+// any P.V reads P.
 __device__ __forceinline__ bool softmax_tile(const TcParams& p, uint8_t* smem, Misc& ms, WorkerCtx& c, uint32_t tmem,
                              const Unit& un, int t, int nu, float* lacc, float* mref, bool& ninf) {
     const uint32_t ts = tmem + c.lane_off + kTmemS + 32 * c.hf;
     const bool valid = t * 128 + c.key < un.n_valid;
+    const bool seeded = t == 0 && c.sinks;
     float x[32];
     if (t == 0) {
-        load_scores(ts, valid, p.scale_log2, x);
-        if (!new_reference<true>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
-        ninf = any_ninf(mref);
+        if (seeded) {
+            // publish the sink references for the output warps, once they
+            // have read the previous unit's
+            ninf = false;
+            if (c.qd == 0) {
+                if (nu > 0 && !mbar_wait(smem_addr(&ms.l_free), (nu - 1) & 1, &ms.abort_flag, p.err)) return false;
+                ms.m_ref[32 * c.hf + c.lane] = sink_ref(p, 32 * c.hf + c.lane);
+            }
+        } else {
+            load_scores(ts, valid, p.scale_log2, x);
+            if (!new_reference<true>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
+            ninf = any_ninf(mref);
+        }
     }
     tmem_ld32(ts, x);
-    // the first tile's references are its maxima: nothing can pass them
-    bool ovf = tile_weights(x, valid, p.scale_log2, mref, ninf) && t > 0;
+    bool ovf;
+    if (seeded) {
+        uint32_t seen;
+        ovf = tile_weights<true>(x, valid, p.scale_log2, mref, false, &seen);
+        seen = __reduce_or_sync(0xffffffffu, seen);
+        if (c.lane == 0 && seen) atomicOr(&ms.seen[c.hf], seen);
+    } else {
+        // an exact first tile's references are its maxima: nothing can pass them
+        ovf = tile_weights(x, valid, p.scale_log2, mref, ninf) && t > 0;
+    }
     ovf = __any_sync(0xffffffffu, ovf);
     store_p(smem, c, x);
-    if (ovf && c.lane == 0) ms.ovf[c.w] = 1;
+    if (ovf && c.lane == 0) ms.ovf = 1;
     if (!publish_p(p, ms, c)) return false;
     if (ms.redo) {
+        if (seeded) {
+            // a sink-seeded first tile is redone with its exact maxima: from
+            // references of -inf they move to the tile's maxima, and nothing
+            // weighted so far needs rescaling
+#pragma unroll
+            for (int h = 0; h < 32; ++h) mref[h] = -INFINITY;
+            if (c.qd == 0) ms.m_ref[32 * c.hf + c.lane] = -INFINITY;
+        }
         load_scores(ts, valid, p.scale_log2, x);
         if (!new_reference<false>(p, ms, c, tmem, x, mref, nu, lacc)) return false;
         ninf = any_ninf(mref);
@@ -556,10 +668,11 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
     c.key = 32 * c.qd + c.lane;
     c.lane_off = static_cast<uint32_t>(32 * c.qd) << 16;
     c.ph_red = c.ph_ack = 0u;
+    c.sinks = sinks_finite(p, c.lane);
     volatile int* ab = &ms.abort_flag;
     const uint32_t sKv = smem_addr(smem + kOffKv);
 
-    int u = blockIdx.x;
+    int u = unit_at(p, ms, 0);
     if (u >= p.units) return;
     Unit un;
     float lacc[32], mref[32];   // this thread's running sums and references (set by each unit's first tile)
@@ -587,8 +700,13 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[c.w < 4 ? 3 : 4]), ph, ab, p.err)) return;
         issue_rows<3>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
+        if (t == 0 && c.sinks) {
+            // the unit starts from the sink references
+#pragma unroll
+            for (int h = 0; h < 32; ++h) mref[h] = sink_ref(p, 32 * c.hf + h);
+        }
         const bool last_tile = t + 1 == un.tiles;
-        const int u_next = last_tile ? u + static_cast<int>(gridDim.x) : u;
+        const int u_next = last_tile ? unit_at(p, ms, nu + 1) : u;
         const bool more = u_next < p.units;
         // 3. scores of this tile
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) return;
@@ -621,23 +739,27 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
 // has issued tile g's gather, so idx[] is free).
 __device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
     volatile int* ab = &ms.abort_flag;
-    int u = blockIdx.x;
+    // with a launch queue this warp takes the CTA's units, one unit ahead
+    int u = p.queue ? take_unit(p, ms, 0, lane) : static_cast<int>(blockIdx.x);
     if (u >= p.units) return;
+    int u_next = p.queue ? take_unit(p, ms, 1, lane) : u + static_cast<int>(gridDim.x);
     prefetch_idx(p, u, 0, ms, lane);
     Unit un = unit_info(p, u);
-    int t = 0, g = 0;
+    int t = 0, g = 0, nu = 0;
     while (true) {
         int u2 = u, t2 = t + 1;
         if (t2 == un.tiles) {
-            u2 = u + static_cast<int>(gridDim.x);
+            u2 = u_next;
             t2 = 0;
         }
         if (u2 >= p.units) break;
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) break;
         prefetch_idx(p, u2, t2, ms, lane);
-        if (u2 != u) {
+        if (t2 == 0) {
             u = u2;
+            ++nu;
             un = unit_info(p, u);
+            u_next = p.queue ? take_unit(p, ms, nu + 1, lane) : u + static_cast<int>(gridDim.x);
         }
         t = t2;
         ++g;
@@ -655,7 +777,9 @@ __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
     const uint32_t q_bytes = 8u * static_cast<uint32_t>(p.H) * 128u;
     const uint32_t bar = smem_addr(&ms.q_full);
     int nu = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+    for (;; ++nu) {
+        const int u = unit_at(p, ms, nu);
+        if (u >= p.units) break;
         if (nu > 0 && !mbar_wait(smem_addr(&ms.q_free), (nu - 1) & 1, ab, p.err)) break;
         mbar_arrive_expect_tx(bar, q_bytes);
         for (int s = 0; s < 8; ++s) tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u / p.chunks) * p.H, bar);
@@ -676,8 +800,9 @@ __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
 __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, int lane) {
     volatile int* ab = &ms.abort_flag;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-    int nu = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++nu) {
+    for (int nu = 0;; ++nu) {
+        const int u = unit_at(p, ms, nu);
+        if (u >= p.units) break;
         if (!mbar_wait(smem_addr(&ms.l_ready), nu & 1, ab, p.err)) return;
         float f[2];     // heads lane and lane + 32
 #pragma unroll
@@ -757,7 +882,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
         mbar_init(smem_addr(&ms.q_free), 1);
         mbar_init(smem_addr(&ms.p_ack), 1);
         mbar_init(smem_addr(&ms.red_sync), kWorkerWarps);
-        for (int w = 0; w < kWorkerWarps; ++w) ms.ovf[w] = 0;
+        ms.ovf = 0;
+        ms.seen[0] = ms.seen[1] = 0;
+        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&ms.unit_full[i]), 1);
         ms.redo = 0;
         mbar_init(smem_addr(&ms.drain), 1);
         mbar_init(smem_addr(&ms.idx_full), 32);
@@ -804,8 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
         regs_dec<kRegsOther>();
         if (warp == kQWarp && (threadIdx.x & 31) == 0) q_role(p, smem, ms);
         if (warp == kIdxWarp) idx_role(p, ms, threadIdx.x & 31);
+        // the whole warp tests the sinks, one thread issues
+        const bool sinks = warp == kMmaWarp && sinks_finite(p, threadIdx.x & 31);
         if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
-            mma_role(p, smem, ms, tmem);
+            mma_role(p, smem, ms, tmem, sinks);
             // every MMA this thread issued has completed before TMEM is freed
             umma_commit(smem_addr(&ms.drain));
             int dummy = 0;
@@ -819,6 +948,15 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (p.queue && threadIdx.x == 0) {
+        // every CTA has taken its last ticket: the last one out (even after
+        // an abort) leaves the queue at zero for the next launch
+        __threadfence();
+        if (atomicAdd(p.queue + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(p.queue, 0);
+            atomicExch(p.queue + 1, 0);
+        }
     }
 }
 

@@ -33,13 +33,20 @@
  *   parallelism); the row width is fixed at 512.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *   default stream) and run on the current device.  The library allocates
- *   nothing per call: a 4-byte device error word and, for decode, one scratch
- *   buffer for split partial results are allocated once per device on first
- *   use (the scratch grows when a larger batch needs it) and released by
- *   dsa_shutdown().  Do not issue the first call of a device inside a CUDA
- *   graph capture.  Decode calls whose work overlaps on the GPU (other
- *   streams, other threads) share that scratch and race; order them on one
- *   stream.
+ *   nothing per call: a small device block (the error word and up to 64
+ *   two-int row queues) and, for decode, one scratch buffer for split partial
+ *   results are allocated once per device on first use (the scratch grows
+ *   when a larger batch needs it) and released by dsa_shutdown().  Do not
+ *   issue the first call of a device inside a CUDA graph capture.  Decode
+ *   calls whose work overlaps on the GPU (other streams, other threads) share
+ *   that scratch and race; order them on one stream.
+ * - A bf16 prefill call with more rows than the GPU has SMs hands its rows to
+ *   the SMs from a row queue owned by its stream (calls on one stream run in
+ *   order; calls on different streams use different queues), so that faster
+ *   SMs take more rows.  It falls back to a fixed round-robin assignment on
+ *   the per-thread default stream, while its stream is being captured into
+ *   a CUDA graph, and once 64 streams of the device hold a queue (until
+ *   dsa_shutdown()).  Which SM runs a row does not change its result.
  * - The kernels are launched with programmatic stream serialisation: a
  *   kernel may start its set-up while the previous work on the stream is
  *   finishing, but it touches no global memory before that work has
@@ -53,7 +60,10 @@
  *   inputs run on the tensor cores (bf16 products, fp32 accumulation, the
  *   softmax weights split into two bf16 terms), fp32 softmax.  Results are
  *   bit-identical from run to run and do not depend on the other rows of the
- *   batch.
+ *   batch.  The bf16 path weighs keys against a per-head reference that may
+ *   lag the running maximum by up to 2^32, so its fp32 sums overflow (to
+ *   +-inf or NaN) only when a selected kv value exceeds about 1e26 in
+ *   magnitude.
  */
 #ifndef DSA_H
 #define DSA_H

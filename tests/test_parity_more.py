@@ -99,3 +99,25 @@ def test_graph_replay_and_side_stream_match_direct_calls(mode):
     assert np.array_equal(a, replayed.cpu().numpy().view(np.uint32))
     ref, _ = oracle.attn(case)
     compare(case, direct.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_sinks_far_above_every_score(mode):
+    # Heads 0-15 carry a sink logit of +80: every score of theirs lies more
+    # than 100 log2 units below it, so weights taken against the sink would
+    # fall to the bottom of the fp32 range.  The outputs of those heads are
+    # tiny (about e^-80 times a mean of V) and must still match relatively.
+    rng = np.random.default_rng(4500)
+    case = I._edge_base(rng, "sink_high_" + mode, I.BF16, 64, 640, mode, R=3, N=2048, k_extra=0)
+    case.sink[:16] = 80.0
+    _check(case)
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_scores_far_above_the_sinks(mode):
+    # Sinks of -60: the first tile's scores pass the sinks by about 86 log2
+    # units, more than a reference may lag.
+    rng = np.random.default_rng(4600)
+    case = I._edge_base(rng, "sink_low_" + mode, I.BF16, 64, 640, mode, R=3, N=2048, k_extra=0)
+    case.sink[:] = -60.0
+    _check(case)
