@@ -121,3 +121,23 @@ def test_scores_far_above_the_sinks(mode):
     case = I._edge_base(rng, "sink_low_" + mode, I.BF16, 64, 640, mode, R=3, N=2048, k_extra=0)
     case.sink[:] = -60.0
     _check(case)
+
+
+def test_decode_rows_match_across_combine_paths():
+    # 40 rows x 5 chunks = 200 partials: more units than SMs, so the chunks
+    # merge through the scratch and the combine kernel.  The first 20 rows
+    # alone (100 units, one wave) merge on chip in thread-block clusters, and
+    # the first 5 rows alone do too, each (row, chunk) split in two column
+    # halves.  A row must give the same bits on every path.
+    rng = np.random.default_rng(4700)
+    big = I._edge_base(rng, "decode_b40", I.BF16, 64, 640, "decode", R=40, N=2048, k_extra=0)
+    full, code = run(big)
+    assert code == 0
+    ref, _ = oracle.attn(big)
+    compare(big, full, ref)
+    for n in (20, 5):
+        sub = I.Case("sub%d" % n, "decode", big.dtype, n, big.H, big.N, big.k_max, big.q[:n], big.kv[:n],
+                     big.idx[:n], big.n_sel[:n], big.sink, big.scale)
+        got, code = run(sub)
+        assert code == 0
+        assert np.array_equal(got.view(np.uint32), full[:n].view(np.uint32))
