@@ -80,18 +80,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // ---------------------------------------------------------------------- TMA
-// Four rows (row0..row3) of one 2-D tensor, columns [col, col + box width),
-// into consecutive box rows at dst; completion is counted on `bar`.  Rows
-// outside the tensor read as zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int col, int row0, int row1,
-                                            int row2, int row3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tmap), "r"(col), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(bar)
-        : "memory");
-}
-
 // One box of a 2-D tensor starting at (col, row) into dst.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int col, int row,
                                             uint32_t bar) {
@@ -168,20 +156,11 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// umma_bf16 with the operand descriptors given as a base plus compile-time
-// offsets (in 16-byte units), added inside the instruction sequence: the issue
-// loop stays a handful of instructions per MMA and nothing is hoisted.
+// D[tmem] (+)= A[smem] * B[smem]^T (bf16 inputs, fp32 accumulation), with
+// the operand descriptors given as a base plus compile-time offsets (in
+// 16-byte units), added inside the instruction sequence: the issue loop stays
+// a handful of instructions per MMA and nothing is hoisted.  accumulate == 0
+// overwrites D.
 template <uint32_t kAOff, uint32_t kBOff>
 __device__ __forceinline__ void umma_bf16_at(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -216,14 +195,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// The value unchanged, but opaque to the compiler: keeps it from hoisting
-// many precomputed descriptors out of a loop (and spilling them).
-__device__ __forceinline__ uint64_t opaque64(uint64_t v) {
-    uint64_t r;
-    asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(v));
-    return r;
-}
-
 // Instruction descriptor for kind::f16 with bf16 A/B and an f32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4)                                     // D format: f32
@@ -255,37 +226,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Two loads of 32 consecutive TMEM columns each (at ta and tb) with one
-// wait for both.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* a, float* b) {
-    uint32_t r[64];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]),
-          "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]),
-          "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]),
-          "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
-          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(ta), "r"(tb)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        a[i] = __uint_as_float(r[i]);
-        b[i] = __uint_as_float(r[32 + i]);
-    }
-}
-
 // 32 lanes x 16 consecutive 32-bit columns, then wait for the load.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
@@ -300,14 +240,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Maximum of v over the 32 lanes of the warp, returned to every lane (NaN
-// inputs are skipped, as fmaxf does).
-__device__ __forceinline__ float warp_max_f32(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on
