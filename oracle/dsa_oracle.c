@@ -167,3 +167,48 @@ int dsa_oracle_attn(const void* q, const void* kv, const int32_t* idx,
     free(heads);
     return rc;
 }
+
+/* ------------------------------------------------------------- top-k */
+typedef struct {
+    float s;
+    int32_t pos;
+} sel_t;
+
+/* The selection order of dsa_oracle_topk: non-NaN before NaN, then larger
+ * score first (IEEE comparison, so -0 == +0), then smaller position. */
+static int sel_cmp(const void* a, const void* b) {
+    const sel_t* x = (const sel_t*)a;
+    const sel_t* y = (const sel_t*)b;
+    const int xn = isnan(x->s), yn = isnan(y->s);
+    if (xn != yn) return xn - yn;
+    if (!xn) {
+        if (x->s > y->s) return -1;
+        if (x->s < y->s) return 1;
+    }
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, int k,
+                    int k_max, int32_t* idx, int32_t* n_sel, int32_t* bad) {
+    if (R < 0 || ld < 0 || k < 1 || k > k_max) return 1;
+    if (R == 0) return 0;
+    if (!scores || !n_valid || !idx || !n_sel) return 1;
+    sel_t* buf = (sel_t*)malloc(sizeof(sel_t) * (size_t)(ld > 0 ? ld : 1));
+    if (!buf) return 1;
+    int r, j;
+    for (r = 0; r < R; ++r) {
+        const int n = n_valid[r];
+        const int ok = n >= 0 && n <= ld;
+        if (bad) bad[r] = ok ? 0 : 1;
+        const int m = ok ? (n < k ? n : k) : 0;
+        for (j = 0; ok && j < n; ++j) {
+            buf[j].s = scores[(size_t)r * (size_t)ld + (size_t)j];
+            buf[j].pos = j;
+        }
+        if (ok && n > 1) qsort(buf, (size_t)n, sizeof(sel_t), sel_cmp);
+        for (j = 0; j < k_max; ++j) idx[(size_t)r * (size_t)k_max + (size_t)j] = j < m ? buf[j].pos : -1;
+        n_sel[r] = m;
+    }
+    free(buf);
+    return 0;
+}

@@ -65,6 +65,30 @@ int dsa_oracle_pairs(const void* q, const void* kv, const int32_t* idx,
 /* Threads an all-thread call would use. */
 int dsa_oracle_max_threads(void);
 
+/*
+ * Top-k selection of an indexer's scores (the "merge and finish" that turns
+ * a row's index scores into the selection the attention reads: DeepSeek
+ * V4.1 indexer PR #2, title: the indexer's merge and finish on a threadgroup
+ * a row, the same picks).  The pages give the title only; the reading is:
+ *
+ *   candidates of row r: positions j in [0, n_valid[r]) with score s[r][j]
+ *   order: larger score first; NaN after every number (also after -inf);
+ *          -0 and +0 are equal; equal scores by smaller position first
+ *   n_sel[r] = min(k, n_valid[r]); idx[r][0 .. n_sel) = the first n_sel
+ *   candidates in that order; idx[r][n_sel .. k_max) = -1.
+ *
+ * Library contract case (not from the pages): a row whose n_valid is outside
+ * [0, ld] selects nothing (n_sel 0, idx all -1) and is reported in bad[r]
+ * (1, else 0).
+ *
+ * Layouts: scores [R][ld] float32 (row r starts at r * ld), n_valid [R],
+ * idx [R][k_max] int32, n_sel [R] int32, bad [R] int32 (may be null).
+ * Returns 0, or 1 on an invalid argument (null pointer, k < 1, k > k_max,
+ * ld < 0, R < 0).
+ */
+int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, int k,
+                    int k_max, int32_t* idx, int32_t* n_sel, int32_t* bad);
+
 #ifdef __cplusplus
 }
 #endif

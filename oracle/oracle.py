@@ -56,6 +56,8 @@ def load():
             for f in (lib.dsa_oracle_rowhead, lib.dsa_oracle_attn, lib.dsa_oracle_pairs):
                 f.restype = I
             lib.dsa_oracle_max_threads.restype = I
+            lib.dsa_oracle_topk.argtypes = [P, I, P, I, I, I, P, P, P]
+            lib.dsa_oracle_topk.restype = I
             _lib = lib
     return _lib
 
@@ -118,3 +120,23 @@ def rowhead(case, r: int, h: int):
 
 def max_threads() -> int:
     return int(load().dsa_oracle_max_threads())
+
+
+def topk(scores, n_valid, k: int, k_max: int = None):
+    """Top-k selection of each row of ``scores`` [R, ld] (see dsa_oracle.h).
+
+    Returns (idx int32 [R, k_max], n_sel int32 [R], bad int32 [R])."""
+    lib = load()
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    if scores.ndim != 2:
+        raise ValueError("scores must be [rows, ld]")
+    R, ld = scores.shape
+    k_max = k if k_max is None else k_max
+    n_valid = np.ascontiguousarray(n_valid, dtype=np.int32)
+    idx = np.empty((R, k_max), np.int32)
+    n_sel = np.empty(R, np.int32)
+    bad = np.empty(R, np.int32)
+    rc = lib.dsa_oracle_topk(_ptr(scores), ld, _ptr(n_valid), R, k, k_max, _ptr(idx), _ptr(n_sel), _ptr(bad))
+    if rc:
+        raise ValueError("oracle rejected its arguments")
+    return idx, n_sel, bad
