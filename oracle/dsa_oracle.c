@@ -188,6 +188,11 @@ static int sel_cmp(const void* a, const void* b) {
     return (x->pos > y->pos) - (x->pos < y->pos);
 }
 
+static int pos_cmp(const void* a, const void* b) {
+    const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
 int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, int k,
                     int k_max, int32_t* idx, int32_t* n_sel, int32_t* bad) {
     if (R < 0 || ld < 0 || k < 1 || k > k_max) return 1;
@@ -206,7 +211,11 @@ int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, 
             buf[j].pos = j;
         }
         if (ok && n > 1) qsort(buf, (size_t)n, sizeof(sel_t), sel_cmp);
-        for (j = 0; j < k_max; ++j) idx[(size_t)r * (size_t)k_max + (size_t)j] = j < m ? buf[j].pos : -1;
+        /* the picks, listed by ascending position */
+        int32_t* out = idx + (size_t)r * (size_t)k_max;
+        for (j = 0; j < m; ++j) out[j] = buf[j].pos;
+        if (m > 1) qsort(out, (size_t)m, sizeof(int32_t), pos_cmp);
+        for (j = m; j < k_max; ++j) out[j] = -1;
         n_sel[r] = m;
     }
     free(buf);

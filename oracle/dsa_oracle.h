@@ -74,8 +74,11 @@ int dsa_oracle_max_threads(void);
  *   candidates of row r: positions j in [0, n_valid[r]) with score s[r][j]
  *   order: larger score first; NaN after every number (also after -inf);
  *          -0 and +0 are equal; equal scores by smaller position first
- *   n_sel[r] = min(k, n_valid[r]); idx[r][0 .. n_sel) = the first n_sel
- *   candidates in that order; idx[r][n_sel .. k_max) = -1.
+ *   n_sel[r] = min(k, n_valid[r]); the picks are the first n_sel candidates
+ *   in that order; idx[r][0 .. n_sel) = the picks in ascending position
+ *   (the attention reads a set: its sum does not depend on the order, and
+ *   ascending positions are its one canonical listing);
+ *   idx[r][n_sel .. k_max) = -1.
  *
  * Library contract case (not from the pages): a row whose n_valid is outside
  * [0, ld] selects nothing (n_sel 0, idx all -1) and is reported in bad[r]

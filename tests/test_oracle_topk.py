@@ -16,11 +16,11 @@ import oracle
 
 def python_topk(row, n, k):
     """The definition written out: (NaN last, larger score first, smaller
-    position first), the first min(k, n) positions."""
+    position first), the first min(k, n) positions, listed ascending."""
     def key(j):
         s = float(row[j])
         return (math.isnan(s), 0.0 if math.isnan(s) else -s, j)
-    return sorted(range(n), key=key)[:min(k, n)]
+    return sorted(sorted(range(n), key=key)[:min(k, n)])
 
 
 def special_scores(rng, n):
@@ -65,13 +65,14 @@ def test_matches_numpy_lexsort_on_a_prefill_row_set(lib):
     idx, n_sel, _ = oracle.topk(scores, n_valid, k)
     for r in range(R):
         n = n_valid[r]
-        order = np.lexsort((np.arange(n), -scores[r, :n]))[:min(k, n)]
+        order = np.sort(np.lexsort((np.arange(n), -scores[r, :n]))[:min(k, n)])
         assert n_sel[r] == min(k, n)
         assert np.array_equal(idx[r, :n_sel[r]], order)
 
 
 def test_selection_properties(lib):
-    # catches: a duplicated or missing pick, an order that is not descending
+    # catches: a duplicated or missing pick, picks not listed ascending, a
+    # pick below a candidate left out
     rng = np.random.default_rng(8)
     ld, k = 2048, 300
     scores = rng.standard_normal((3, ld), dtype=np.float32)
@@ -79,10 +80,9 @@ def test_selection_properties(lib):
     for r in range(3):
         sel = idx[r, :k]
         assert len(set(sel.tolist())) == k and sel.min() >= 0 and sel.max() < ld
-        s = scores[r, sel]
-        assert (np.diff(s) <= 0).all()
+        assert (np.diff(sel) > 0).all()
         rest = np.setdiff1d(np.arange(ld), sel)
-        assert s.min() >= scores[r, rest].max()
+        assert scores[r, sel].min() >= scores[r, rest].max()
 
 
 def test_all_equal_scores_pick_the_first_positions(lib):
@@ -98,7 +98,7 @@ def test_fewer_candidates_than_k_take_all_in_order(lib):
     scores = np.array([[0.5, -1.0, 2.0, np.nan, 2.0, 0.0]], np.float32)
     idx, n_sel, _ = oracle.topk(scores, np.array([6], np.int32), 10)
     assert n_sel[0] == 6
-    assert list(idx[0, :6]) == [2, 4, 0, 5, 1, 3]
+    assert list(idx[0, :6]) == [0, 1, 2, 3, 4, 5]
     assert (idx[0, 6:] == -1).all()
 
 
@@ -106,7 +106,9 @@ def test_nan_only_when_numbers_run_out(lib):
     # catches: NaN compared as a number
     scores = np.array([[np.nan, -np.inf, np.nan, -np.inf]], np.float32)
     idx, n_sel, _ = oracle.topk(scores, np.array([4], np.int32), 3)
-    assert list(idx[0]) == [1, 3, 0]
+    assert list(idx[0]) == [0, 1, 3]
+    idx, n_sel, _ = oracle.topk(scores, np.array([4], np.int32), 2)
+    assert list(idx[0]) == [1, 3]
 
 
 def test_bad_n_valid_selects_nothing(lib):
