@@ -224,6 +224,35 @@ def decode_sustained(dsa, d, case, dev):
     return e0.elapsed_time(e1) / (reps * SUS_CALLS)
 
 
+def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
+    """Mean milliseconds of one top-k selection call over the indexer-score
+    rows of `mode` (prefill: 2048 causal rows of a 4096 cache; decode: 8
+    rows of 32768), the L2 flushed before each call; and the bytes of
+    scores it reads."""
+    import torch
+    scores, n_valid = I.indexer_scores(mode)
+    s = torch.from_numpy(scores).to(dev)
+    nv = torch.from_numpy(n_valid).to(dev)
+    R = scores.shape[0]
+    idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(R, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert dsa.dsa_get_device_error() == 0
+    return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
+
+
 def bench_ours(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
@@ -361,6 +390,16 @@ def bench_ours(args, world, rank, local):
             "gathered_frac_hbm": g / (dec_sus_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "how": "%d calls back to back from one CUDA graph over %d rotating q/idx/out sets; "
                    "no L2 flush (the 256 MiB of caches exceed L2)" % (SUS_CALLS, SUS_SETS)}
+    if args.workload == "both":
+        # the indexer's top-k selection, timed on its own (not part of the step)
+        for mode, key in (("prefill", "topk_prefill_2048"), ("decode", "topk_decode_b8")):
+            t_ms, rows, nbytes = topk_timing(dsa, dev, flush, mode)
+            t_ms = reduce_max(t_ms, world)
+            workloads[key] = {
+                "ms": t_ms, "rows_per_s": rows / (t_ms * 1e-3),
+                "scores_gbs": nbytes / (t_ms * 1e-3) / 1e9,
+                "scores_frac_hbm": nbytes / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "how": "dsa_topk_select, k=%d, N(0,1) scores, one call a time, L2 flushed before each" % K}
     roofline = None
     if do_pre:
         g = PRE_R * K * D * 2

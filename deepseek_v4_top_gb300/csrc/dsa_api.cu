@@ -214,6 +214,30 @@ dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache, const in
     return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, false);
 }
 
+dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, int R, int k,
+                           int32_t* idx, int k_max, int32_t* n_sel, void* stream) {
+    if (R < 0 || k < 1 || k_max < k || ld < 1 || (ld & 3) != 0) return DSA_ERR_INVALID_ARG;
+    if (k > dsa::kTopkMaxK || ld > dsa::kTopkMaxLd) return DSA_ERR_UNSUPPORTED;
+    if (R == 0) return DSA_OK;
+    if (!scores || !n_valid || !idx || !n_sel) return DSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(scores) & 15u) != 0) return DSA_ERR_INVALID_ARG;
+    dsa::DeviceState* ds = nullptr;
+    dsa_status st = dsa::device_state(&ds);
+    if (st != DSA_OK) return st;
+    dsa::TopkParams p;
+    p.scores = scores;
+    p.n_valid = n_valid;
+    p.idx = idx;
+    p.n_sel = n_sel;
+    p.err = ds->err;
+    p.R = R;
+    p.ld = ld;
+    p.k = k;
+    p.k_max = k_max;
+    const int grid = R < (1 << 20) ? R : (1 << 20);
+    return dsa::launch_topk(p, grid, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 dsa_status dsa_get_device_error(void* stream, uint32_t* code) {
     if (!code) return DSA_ERR_INVALID_ARG;
     dsa::DeviceState* ds = nullptr;

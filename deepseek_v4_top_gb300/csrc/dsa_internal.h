@@ -76,6 +76,22 @@ inline int column_halves(int partial, int parts, int sm_count) {
     return partial && 2LL * parts <= sm_count ? 2 : 1;
 }
 
+// One launch of the top-k selection kernel (dsa_topk.cu).
+struct TopkParams {
+    const float* scores;      // [R][ld] (ld a multiple of 4, rows 16-byte aligned)
+    const int32_t* n_valid;   // [R]: row r's candidates are positions [0, n_valid[r])
+    int32_t* idx;             // [R][k_max]
+    int32_t* n_sel;           // [R]
+    uint32_t* err;            // device error word
+    int R, ld, k, k_max;
+};
+
+// Largest k and row length the top-k kernel takes (a row's keys are held in
+// the registers of one CTA).
+constexpr int kTopkMaxK = 2048;
+constexpr int kTopkMaxLd = 32768;
+cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t s);
+
 // Shared memory of the tensor-core kernel (bytes, dynamic).
 size_t tc_smem_bytes();
 

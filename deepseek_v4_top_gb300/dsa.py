@@ -28,10 +28,11 @@ DSA_DEVERR_IDX_RANGE = 0x1
 DSA_DEVERR_NSEL_RANGE = 0x2
 DSA_DEVERR_TIMEOUT = 0x4
 DSA_DEVERR_LAYOUT = 0x8
+DSA_DEVERR_NVALID_RANGE = 0x10
 
 # Every function declared in include/dsa.h.
 EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_sparse_attn_decode_noalloc",
-           "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
+           "dsa_topk_select", "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
 DSA_NOALLOC_MAX_UNITS = 64
 
 _lib = None
@@ -59,6 +60,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = sig
                 fn.restype = I
+            lib.dsa_topk_select.argtypes = [P, I, P, I, I, P, I, P, P]
+            lib.dsa_topk_select.restype = I
             lib.dsa_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             lib.dsa_get_device_error.restype = I
             lib.dsa_status_string.argtypes = [I]
@@ -158,6 +161,27 @@ def dsa_sparse_attn_decode_noalloc(q, kv_cache, idx, n_sel, sink, scale, out, st
     see include/dsa.h for its size limit and its sharing rules)."""
     return _run("dsa_sparse_attn_decode_noalloc", True, q, kv_cache, idx, n_sel, sink, scale, out,
                 stream)
+
+
+def dsa_topk_select(scores, n_valid, k, idx, n_sel, stream=None):
+    """Top-k selection of each row of scores [R, ld] (float32) among positions
+    [0, n_valid[r]) into idx [R, k_max] and n_sel [R] (int32)."""
+    import torch
+    for name, t in (("scores", scores), ("n_valid", n_valid), ("idx", idx), ("n_sel", n_sel)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if scores.dtype != torch.float32 or scores.dim() != 2:
+        raise TypeError("scores must be a float32 [rows, ld] tensor")
+    if n_valid.dtype != torch.int32 or idx.dtype != torch.int32 or n_sel.dtype != torch.int32:
+        raise TypeError("n_valid, idx and n_sel must be int32")
+    R, ld = scores.shape
+    if tuple(n_valid.shape) != (R,) or tuple(n_sel.shape) != (R,) or idx.dim() != 2 or idx.shape[0] != R:
+        raise ValueError("n_valid [rows], idx [rows, k_max] and n_sel [rows] expected")
+    st = load().dsa_topk_select(scores.data_ptr(), ld, n_valid.data_ptr(), R, int(k), idx.data_ptr(),
+                                idx.shape[1], n_sel.data_ptr(), _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_topk_select")
+    return idx, n_sel
 
 
 def dsa_get_device_error(stream=None) -> int:

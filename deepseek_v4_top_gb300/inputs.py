@@ -215,6 +215,29 @@ def prefill(seed: Optional[int] = None, rows: int = 2048, N: int = 4096,
                 sink, 1.0 / math.sqrt(D))
 
 
+def indexer_scores(mode: str = "prefill", seed: Optional[int] = None, rows: Optional[int] = None,
+                   N: Optional[int] = None):
+    """Index scores for the top-k selection: N(0,1) float32 per (row, position).
+
+    prefill: 2048 rows at positions N-2048 .. N-1 of an N = 4096 cache; row i
+    has n_valid = p + 1 candidates (its causal prefix).  decode: 8 rows, each
+    over its own 32768-position cache (n_valid = N).  Returns
+    (scores [rows, N], n_valid [rows]).
+    """
+    s = SEED_BASE + (5 if mode == "prefill" else 6) if seed is None else seed
+    rng = np.random.default_rng(s)
+    if mode == "prefill":
+        rows = 2048 if rows is None else rows
+        N = 4096 if N is None else N
+        n_valid = (np.arange(rows) + (N - rows) + 1).astype(np.int32)
+    else:
+        rows = 8 if rows is None else rows
+        N = 32768 if N is None else N
+        n_valid = np.full(rows, N, np.int32)
+    scores = rng.standard_normal((rows, N), dtype=np.float32)
+    return scores, n_valid
+
+
 EDGE_HEADS = (16, 32, 64)
 EDGE_KS = (1, 7, 63, 64, 65, 127, 640)
 EDGE_SPECIALS = ("q_nan", "q_pinf", "q_ninf", "kv_nan", "kv_pinf", "kv_ninf",

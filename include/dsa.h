@@ -100,6 +100,8 @@ typedef enum {
                                        outputs of that launch are undefined      */
 #define DSA_DEVERR_LAYOUT     0x8u  /* shared memory not 1024-byte aligned; the
                                        kernel did no work                        */
+#define DSA_DEVERR_NVALID_RANGE 0x10u /* dsa_topk_select: an n_valid entry outside
+                                       [0, ld]; that row selects nothing         */
 
 /*
  * Decode: B slots with one query row each.  Row b attends to k <= k_max
@@ -164,6 +166,34 @@ DSA_API dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_
                                                   const float* sink, float scale, float* out,
                                                   int B, int H, int N, int k_max,
                                                   dsa_dtype dtype, void* stream);
+
+/*
+ * Top-k selection of an indexer's scores: the step that turns a row's index
+ * scores into the selection the attention calls above read (DeepSeek V4.1
+ * indexer PR #2, title: the indexer's merge and finish on a threadgroup a
+ * row, the same picks; the pages give no more, and the order below is this
+ * library's reading).
+ *   scores  [R][ld] float32; row r's candidates are positions
+ *           [0, n_valid[r]).  16-byte aligned; ld a multiple of 4,
+ *           1 <= ld <= 32768.
+ *   n_valid [R] int32
+ *   idx     [R][k_max] int32 out: the picks of row r by ascending
+ *           position, then -1
+ *   n_sel   [R] int32 out: min(k, n_valid[r])
+ * The picks are the first min(k, n_valid[r]) candidates in this order:
+ * larger score first; NaN after every number (also after -inf); -0 and +0
+ * equal; equal scores by smaller position first.  They are listed by
+ * ascending position (the attention reads a set).  1 <= k <= k_max,
+ * k <= 2048.  idx and n_sel can be passed straight to the attention calls.
+ * An n_valid[r] outside [0, ld] sets DSA_DEVERR_NVALID_RANGE, and that row
+ * selects nothing (n_sel 0, idx all -1).  Asynchronous on `stream`; reads
+ * no input before the work queued before it on the stream has completed.
+ * DSA_ERR_INVALID_ARG for a null pointer, a misaligned scores, or bad
+ * sizes; DSA_ERR_UNSUPPORTED for k > 2048 or ld > 32768.
+ */
+DSA_API dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, int R,
+                                   int k, int32_t* idx, int k_max, int32_t* n_sel,
+                                   void* stream);
 
 /*
  * Synchronises `stream`, stores the current device's error word in *code

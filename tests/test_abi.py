@@ -86,3 +86,25 @@ def test_host_validation_before_any_launch(lib, name):
 
 def test_device_error_query_rejects_null(lib):
     assert lib.dsa_get_device_error(None, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_topk_host_validation_before_any_launch(lib):
+    good = dict(scores=FAKE, ld=64, n_valid=FAKE, R=3, k=8, idx=FAKE, k_max=8, n_sel=FAKE)
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        return lib.dsa_topk_select(a["scores"], a["ld"], a["n_valid"], a["R"], a["k"], a["idx"],
+                                   a["k_max"], a["n_sel"], None)
+
+    for ptr in ("scores", "n_valid", "idx", "n_sel"):
+        assert call(**{ptr: 0}) == dsa.DSA_ERR_INVALID_ARG
+    assert call(scores=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG     # misaligned rows
+    assert call(ld=62) == dsa.DSA_ERR_INVALID_ARG                # not a multiple of 4
+    assert call(ld=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(k=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(k=9) == dsa.DSA_ERR_INVALID_ARG                 # k > k_max
+    assert call(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert call(k=2049, k_max=4096) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(ld=32772) == dsa.DSA_ERR_UNSUPPORTED
+    assert call(R=0, scores=0) == dsa.DSA_OK
