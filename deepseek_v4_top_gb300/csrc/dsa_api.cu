@@ -238,6 +238,14 @@ dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, 
     return dsa::launch_topk(p, grid, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+dsa_status dsa_selftest_wait_limit(void* stream) {
+    dsa::DeviceState* ds = nullptr;
+    dsa_status st = dsa::device_state(&ds);
+    if (st != DSA_OK) return st;
+    return dsa::launch_wait_selftest(ds->err, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSA_OK
+                                                                                            : DSA_ERR_CUDA;
+}
+
 dsa_status dsa_get_device_error(void* stream, uint32_t* code) {
     if (!code) return DSA_ERR_INVALID_ARG;
     dsa::DeviceState* ds = nullptr;

@@ -98,5 +98,6 @@ size_t tc_smem_bytes();
 cudaError_t launch_tc(const TcParams& p, int grid, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
 
 }  // namespace dsa

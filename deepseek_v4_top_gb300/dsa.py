@@ -32,7 +32,8 @@ DSA_DEVERR_NVALID_RANGE = 0x10
 
 # Every function declared in include/dsa.h.
 EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_sparse_attn_decode_noalloc",
-           "dsa_topk_select", "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
+           "dsa_topk_select", "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string",
+           "dsa_shutdown")
 DSA_NOALLOC_MAX_UNITS = 64
 
 _lib = None
@@ -62,6 +63,8 @@ def load():
                 fn.restype = I
             lib.dsa_topk_select.argtypes = [P, I, P, I, I, P, I, P, P]
             lib.dsa_topk_select.restype = I
+            lib.dsa_selftest_wait_limit.argtypes = [P]
+            lib.dsa_selftest_wait_limit.restype = I
             lib.dsa_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             lib.dsa_get_device_error.restype = I
             lib.dsa_status_string.argtypes = [I]
@@ -182,6 +185,13 @@ def dsa_topk_select(scores, n_valid, k, idx, n_sel, stream=None):
     if st != DSA_OK:
         raise DsaError(st, "dsa_topk_select")
     return idx, n_sel
+
+
+def dsa_selftest_wait_limit(stream=None) -> None:
+    """Queue the bounded-wait self-test (sets DSA_DEVERR_TIMEOUT after ~2 s)."""
+    st = load().dsa_selftest_wait_limit(_stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_selftest_wait_limit")
 
 
 def dsa_get_device_error(stream=None) -> int:

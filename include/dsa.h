@@ -196,6 +196,17 @@ DSA_API dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n
                                    void* stream);
 
 /*
+ * Self-test of the bounded waits (the pages have no counterpart): queues on
+ * `stream` one small kernel whose only wait is on a barrier that nothing
+ * completes.  After the library's wait limit (about 2 seconds) the wait gives
+ * up, sets DSA_DEVERR_TIMEOUT in the device error word and the kernel
+ * returns; the context stays usable.  Every wait in the attention and
+ * selection kernels is bounded the same way, so a fault on the GPU's side
+ * shows up as an error bit, never as a hang.
+ */
+DSA_API dsa_status dsa_selftest_wait_limit(void* stream);
+
+/*
  * Synchronises `stream`, stores the current device's error word in *code
  * and clears it.  *code is 0 when no launch since the last read found a
  * problem.  DSA_ERR_INVALID_ARG if code is NULL; DSA_ERR_CUDA if the
