@@ -87,10 +87,12 @@ class Case:
     sink: np.ndarray
     scale: float
     note: str = ""
+    rows_per_slot: int = 1   # decode: query rows sharing a slot (row r reads slot r // rows_per_slot)
 
     @property
     def B(self) -> int:
-        return self.R
+        """Slots of a decode case (rows of a prefill case)."""
+        return self.R // self.rows_per_slot if self.mode == "decode" else self.R
 
     def as_f32(self, a: np.ndarray) -> np.ndarray:
         """Input array widened to float32 (exact for bf16 bits)."""
@@ -98,7 +100,7 @@ class Case:
 
     def kv_rows_of(self, r: int) -> np.ndarray:
         """The cache that row r selects from (widened to float32)."""
-        base = self.kv[r] if self.mode == "decode" else self.kv
+        base = self.kv[r // self.rows_per_slot] if self.mode == "decode" else self.kv
         return self.as_f32(base)
 
     def gathered_bytes(self) -> int:
@@ -213,6 +215,35 @@ def prefill(seed: Optional[int] = None, rows: int = 2048, N: int = 4096,
     sink = rng.standard_normal(H, dtype=np.float32)
     return Case("prefill", "prefill", BF16, rows, H, N, k, q, kv, idx, n_sel,
                 sink, 1.0 / math.sqrt(D))
+
+
+def multi_row_decode(seed: Optional[int] = None, B: int = 8, T: int = 2, N: int = 32768,
+                     k: int = 640, dtype: str = BF16, H: int = 64) -> Case:
+    """Decode with T query rows a slot (a step's draft tokens verified together).
+
+    Slot b's rows b*T .. b*T+T-1 read cache kv[b].  Row 0 of a slot selects k
+    distinct random positions; each later row of the slot keeps about 90% of
+    them and replaces the rest with other positions, so the rows' selections
+    overlap as those of neighbouring tokens do.
+    """
+    s = SEED_BASE + 7 if seed is None else seed
+    rng = np.random.default_rng(s)
+    R = B * T
+    q = _normal(rng, (R, H, D), dtype)
+    kv = _normal(rng, (B, N, D), dtype)
+    idx = _empty_idx(R, k)
+    for b in range(B):
+        base = _distinct(rng, N, k)
+        for t in range(T):
+            row = base.copy()
+            if t > 0:
+                swap = rng.random(k) < 0.1
+                fresh = np.setdiff1d(_distinct(rng, N, min(N, 2 * k)), base)[:int(swap.sum())]
+                row[np.nonzero(swap)[0][:len(fresh)]] = fresh
+            idx[b * T + t] = row
+    sink = rng.standard_normal(H, dtype=np.float32)
+    return Case("multi_row_decode", "decode", dtype, R, H, N, k, q, kv, idx,
+                np.full(R, k, np.int32), sink, 1.0 / math.sqrt(D), rows_per_slot=T)
 
 
 def indexer_scores(mode: str = "prefill", seed: Optional[int] = None, rows: Optional[int] = None,

@@ -65,7 +65,8 @@ static void rowhead(const void* q, const void* kv, const int32_t* idx,
     }
 
     const size_t qoff = ((size_t)r * H + h) * DSA_D;
-    const size_t slot = decode ? (size_t)r * (size_t)N * DSA_D : 0;
+    /* decode: T = decode rows share a slot; row r reads slot r / T */
+    const size_t slot = decode ? (size_t)(r / decode) * (size_t)N * DSA_D : 0;
     const double sc = (double)scale;
     const double sk = (double)sink[h];
 

@@ -27,7 +27,10 @@
  *
  * Layouts (row-major, contiguous):
  *   q    [R][H][512]        dtype elements
- *   kv   prefill [N][512]; decode [R][N][512] (row r uses slot r)
+ *   kv   prefill (decode == 0): [N][512], one cache for every row;
+ *        decode == T >= 1: [R/T][N][512], row r uses slot r / T (T query
+ *        rows a slot, e.g. a decode step's draft tokens; T = 1 is the plain
+ *        one-row-per-slot decode)
  *   idx  [R][k_max] int32,  n_sel [R] int32,  sink [H] float32
  *   out  double, [R][H][512] (dsa_oracle_attn) or [n_pairs][512]
  */

@@ -74,7 +74,8 @@ def _common(case):
     sink = np.ascontiguousarray(case.sink, dtype=np.float32)
     keep = (q, kv, idx, n_sel, sink)
     args = [_ptr(q), _ptr(kv), _ptr(idx), _ptr(n_sel), _ptr(sink), ctypes.c_float(case.scale),
-            _DT[case.dtype], 1 if case.mode == "decode" else 0, case.R, case.H, case.N, case.k_max]
+            _DT[case.dtype], case.rows_per_slot if case.mode == "decode" else 0, case.R, case.H, case.N,
+            case.k_max]
     return keep, args
 
 

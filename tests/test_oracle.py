@@ -341,3 +341,16 @@ def test_golden_closed_forms(oracle_lib):
             for d, v in vec.items():
                 expect[int(d)] = float(Fraction(v))
             np.testing.assert_allclose(got[0, h], expect, rtol=4e-16, atol=0, err_msg=g["name"])
+
+
+@pytest.mark.parametrize("T", [2, 3])
+def test_rows_sharing_a_slot_read_that_slot(oracle_lib, T):
+    # catches: a row reading slot r instead of slot r // T
+    c = I.multi_row_decode(B=2, T=T, N=300, k=40, dtype=I.F32, H=4, seed=31)
+    got, _ = oracle_lib.attn(c)
+    kv_each = np.stack([c.kv[r // T] for r in range(c.R)])
+    plain = I.Case("plain", "decode", c.dtype, c.R, c.H, c.N, c.k_max, c.q, kv_each, c.idx, c.n_sel,
+                   c.sink, c.scale)
+    ref, _ = oracle_lib.attn(plain)
+    assert np.array_equal(got, ref)
+    assert c.B == 2
