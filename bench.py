@@ -254,6 +254,32 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
     return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
 
 
+def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
+    """Mean milliseconds of one decode call with T query rows a slot (B slots
+    of a 32768-position cache, k=640), the L2 flushed before each call."""
+    import torch
+    c = I.multi_row_decode(B=B, T=T, N=DEC_N)
+    t = lambda a, bf: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+                       if bf else torch.from_numpy(a).to(dev))
+    q, kv, idx, n_sel, sink = t(c.q, True), t(c.kv, True), t(c.idx, False), t(c.n_sel, False), t(c.sink, False)
+    out = torch.empty((c.R, H, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert dsa.dsa_get_device_error() == 0
+    return sum(ms) / reps, c.R
+
+
 def bench_ours(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
@@ -427,6 +453,16 @@ def bench_ours(args, world, rank, local):
             "how": "%d calls back to back from one CUDA graph over %d rotating q/idx/out sets; "
                    "no L2 flush (the 256 MiB of caches exceed L2)" % (SUS_CALLS, SUS_SETS)}
     if args.workload == "both":
+        # decode with two query rows a slot, timed on its own (not part of the step)
+        t_ms, rows = decode_rows_timing(dsa, dev, flush)
+        t_ms = reduce_max(t_ms, world)
+        g = rows * K * D * 2
+        workloads["decode_b8_t2"] = {
+            "ms": t_ms, "row_heads_per_s": rows * H / (t_ms * 1e-3),
+            "gathered_kv_gbs": g / (t_ms * 1e-3) / 1e9,
+            "gathered_frac_hbm": g / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "how": "dsa_sparse_attn_decode_rows, 8 slots x 2 rows (N=32768 per slot), one call a time, "
+                   "L2 flushed before each"}
         # the indexer's top-k selection, timed on its own (not part of the step)
         for mode, key in (("prefill", "topk_prefill_2048"), ("decode", "topk_decode_b8")):
             t_ms, rows, nbytes = topk_timing(dsa, dev, flush, mode)

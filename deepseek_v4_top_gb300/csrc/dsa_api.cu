@@ -104,7 +104,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
                       const float* sink, const float* out, int R, int H, int N, int k_max,
-                      dsa_dtype dtype, bool decode) {
+                      dsa_dtype dtype, int decode) {
     if (R < 0 || N <= 0 || k_max <= 0 || H <= 0) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
     if (H > kHeadsPad) return DSA_ERR_UNSUPPORTED;   // heads are padded to 64 on chip
@@ -121,9 +121,11 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
     return DSA_OK;
 }
 
+// decode: 0 for prefill (one cache shared by every row), T >= 1 for decode
+// with T query rows a slot (row r reads slot r / T).
 dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
                const float* sink, float scale, float* out, int R, int H, int N, int k_max,
-               dsa_dtype dtype, void* stream, bool decode) {
+               dsa_dtype dtype, void* stream, int decode) {
     dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype, decode);
     if (st != DSA_OK || R == 0) return st;
     DeviceState* ds = nullptr;
@@ -145,7 +147,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
         p.H = H;
         p.N = N;
         p.k_max = k_max;
-        p.decode = decode ? 1 : 0;
+        p.decode = decode;
         return launch_simt(p, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     }
 
@@ -164,7 +166,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     p.H = H;
     p.N = N;
     p.k_max = k_max;
-    p.decode = decode ? 1 : 0;
+    p.decode = decode;
     const int chunks = decode ? (k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys : 1;
     p.chunk_keys = chunks > 1 ? kDecodeChunkKeys : k_max;
     p.chunks = chunks;
@@ -205,13 +207,21 @@ extern "C" {
 dsa_status dsa_sparse_attn_decode(const void* q, const void* kv_cache, const int32_t* idx,
                                   const int32_t* n_sel, const float* sink, float scale, float* out,
                                   int B, int H, int N, int k_max, dsa_dtype dtype, void* stream) {
-    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, B, H, N, k_max, dtype, stream, true);
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, B, H, N, k_max, dtype, stream, 1);
+}
+
+dsa_status dsa_sparse_attn_decode_rows(const void* q, const void* kv_cache, const int32_t* idx,
+                                       const int32_t* n_sel, const float* sink, float scale, float* out,
+                                       int B, int T, int H, int N, int k_max, dsa_dtype dtype,
+                                       void* stream) {
+    if (B < 0 || T < 1 || static_cast<long long>(B) * T > 0x7FFFFFFFLL) return DSA_ERR_INVALID_ARG;
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, B * T, H, N, k_max, dtype, stream, T);
 }
 
 dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache, const int32_t* idx,
                                    const int32_t* n_sel, const float* sink, float scale, float* out,
                                    int R, int H, int N, int k_max, dsa_dtype dtype, void* stream) {
-    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, false);
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, 0);
 }
 
 dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, int R, int k,

@@ -37,7 +37,7 @@ struct TcParams {
                               // queue [next ticket, CTAs finished], zero at launch, left zero
     float scale_log2;         // scale * log2(e)
     int R, H, N, k_max;
-    int decode;               // 1: row r reads slot r
+    int decode;               // 0: prefill (one cache); T >= 1: row r reads slot r / T
     int chunk_keys;           // keys per unit (multiple of 16)
     int chunks;               // key chunks per row
     int halves;               // 1, or 2: each (row, chunk) runs as two units, one per column half
@@ -58,7 +58,7 @@ struct SimtParams {
     uint32_t* err;
     float scale;
     int R, H, N, k_max;
-    int decode;
+    int decode;               // as TcParams::decode
 };
 
 struct CombineParams {

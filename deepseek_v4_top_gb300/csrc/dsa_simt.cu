@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
     const bool bad_n = ns < 0 || ns > p.k_max;
     if (bad_n && h == 0 && tid == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
     const int eff = bad_n ? 1 : ns;
-    const float* cache = p.kv + (p.decode ? static_cast<size_t>(r) * p.N * kD : 0);
+    const float* cache = p.kv + (p.decode ? static_cast<size_t>(r / p.decode) * p.N * kD : 0);
     const float* nan_row = reinterpret_cast<const float*>(kNanRowF32);
 
     float m = -INFINITY, l = 0.0f;

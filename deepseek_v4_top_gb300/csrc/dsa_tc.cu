@@ -290,7 +290,7 @@ template <int q>
 __device__ __forceinline__ void issue_rows(const TcParams& p, const Misc& ms, const Unit& un, int t,
                                           uint32_t sKv, int wt) {
     const int w = wt >> 5, lane = wt & 31, cc = lane & 7;
-    const uint16_t* cache = p.kv + (p.decode ? static_cast<size_t>(un.r) * p.N * kD : 0);
+    const uint16_t* cache = p.kv + (p.decode ? static_cast<size_t>(un.r / p.decode) * p.N * kD : 0);
     const uint16_t* nan_row = reinterpret_cast<const uint16_t*>(kNanRowBf16);
     {
         const int j = 4 * (w + 8 * q) + (lane >> 3);

@@ -31,7 +31,8 @@ DSA_DEVERR_LAYOUT = 0x8
 DSA_DEVERR_NVALID_RANGE = 0x10
 
 # Every function declared in include/dsa.h.
-EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_prefill", "dsa_sparse_attn_decode_noalloc",
+EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_decode_rows", "dsa_sparse_attn_prefill",
+           "dsa_sparse_attn_decode_noalloc",
            "dsa_topk_select", "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string",
            "dsa_shutdown")
 DSA_NOALLOC_MAX_UNITS = 64
@@ -61,6 +62,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = sig
                 fn.restype = I
+            lib.dsa_sparse_attn_decode_rows.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, P]
+            lib.dsa_sparse_attn_decode_rows.restype = I
             lib.dsa_topk_select.argtypes = [P, I, P, I, I, P, I, P, P]
             lib.dsa_topk_select.restype = I
             lib.dsa_selftest_wait_limit.argtypes = [P]
@@ -98,7 +101,7 @@ def _dtype_code(t):
     raise TypeError("q and kv_cache must be float32 or bfloat16, got %s" % t.dtype)
 
 
-def _check(q, kv, idx, n_sel, sink, out, decode):
+def _check(q, kv, idx, n_sel, sink, out, decode, rows_per_slot=1):
     import torch
     for name, t in (("q", q), ("kv_cache", kv), ("idx", idx), ("n_sel", n_sel), ("sink", sink),
                     ("out", out)):
@@ -118,8 +121,8 @@ def _check(q, kv, idx, n_sel, sink, out, decode):
         raise ValueError("q must be [rows, heads, 512]")
     R, H = q.shape[0], q.shape[1]
     if decode:
-        if kv.dim() != 3 or kv.shape[0] != R or kv.shape[2] != 512:
-            raise ValueError("decode kv_cache must be [B, N, 512]")
+        if kv.dim() != 3 or kv.shape[0] * rows_per_slot != R or kv.shape[2] != 512:
+            raise ValueError("decode kv_cache must be [slots, N, 512] with slots * rows_per_slot = rows")
         N = kv.shape[1]
     else:
         if kv.dim() != 2 or kv.shape[1] != 512:
@@ -152,6 +155,24 @@ def _run(name, decode, q, kv_cache, idx, n_sel, sink, scale, out, stream):
 def dsa_sparse_attn_decode(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
     """Decode attention: q [B,H,512], kv_cache [B,N,512], out [B,H,512] fp32."""
     return _run("dsa_sparse_attn_decode", True, q, kv_cache, idx, n_sel, sink, scale, out, stream)
+
+
+def dsa_sparse_attn_decode_rows(q, kv_cache, idx, n_sel, sink, scale, out, rows_per_slot, stream=None):
+    """Decode with T = rows_per_slot query rows a slot: q [B*T,H,512], kv_cache [B,N,512],
+    idx [B*T,k_max], n_sel [B*T], out [B*T,H,512] fp32; row r reads slot r // T."""
+    T = int(rows_per_slot)
+    if T < 1:
+        raise ValueError("rows_per_slot must be >= 1")
+    if kv_cache.dim() != 3 or q.dim() != 3 or q.shape[0] != kv_cache.shape[0] * T:
+        raise ValueError("q must be [slots * rows_per_slot, heads, 512] for kv_cache [slots, N, 512]")
+    R, H, N, k_max = _check(q, kv_cache, idx, n_sel, sink, out, decode=True, rows_per_slot=T)
+    st = load().dsa_sparse_attn_decode_rows(q.data_ptr(), kv_cache.data_ptr(), idx.data_ptr(),
+                                            n_sel.data_ptr(), sink.data_ptr(), ctypes.c_float(float(scale)),
+                                            out.data_ptr(), R // T, T, H, N, k_max, _dtype_code(q),
+                                            _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_sparse_attn_decode_rows")
+    return out
 
 
 def dsa_sparse_attn_prefill(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):

@@ -118,6 +118,23 @@ DSA_API dsa_status dsa_sparse_attn_decode(const void* q, const void* kv_cache,
                                           dsa_dtype dtype, void* stream);
 
 /*
+ * Decode with T query rows a slot: B slots, each with T rows that attend to
+ * the slot's own cache (several tokens of one sequence decoded together, as
+ * when a step's draft tokens are verified).  Row r = b*T + t reads only
+ * kv[b]; every row has its own selection.  T = 1 is dsa_sparse_attn_decode.
+ *   q [B*T][H][512], kv [B][N][512], idx [B*T][k_max], n_sel [B*T],
+ *   out [B*T][H][512].
+ * A row's result is bit-identical to the same row in a one-row-a-slot call
+ * over that slot's cache.  DSA_ERR_INVALID_ARG for T < 1 or B*T beyond int
+ * range; otherwise as dsa_sparse_attn_decode (the split scratch included).
+ */
+DSA_API dsa_status dsa_sparse_attn_decode_rows(const void* q, const void* kv_cache,
+                                               const int32_t* idx, const int32_t* n_sel,
+                                               const float* sink, float scale, float* out,
+                                               int B, int T, int H, int N, int k_max,
+                                               dsa_dtype dtype, void* stream);
+
+/*
  * Prefill: R query rows of one segment attend to one shared cache of N
  * positions (TensorFold PR #1206: 2048-row prefill segments; a row at
  * position p selects min(p+1, k) positions in [0, p]).

@@ -30,8 +30,12 @@ def run(case, dev_inputs=None, dev="cuda:0", check_guards=True):
     buf = torch.empty(n + 2 * GUARD, dtype=torch.int32, device=dev)
     buf.fill_(int(SENTINEL.view(np.int32)))
     out = buf[GUARD:GUARD + n].view(torch.float32).view(case.R, case.H, 512)
-    fn = dsa.dsa_sparse_attn_decode if case.mode == "decode" else dsa.dsa_sparse_attn_prefill
-    fn(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], case.scale, out)
+    if case.mode == "decode" and case.rows_per_slot > 1:
+        dsa.dsa_sparse_attn_decode_rows(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], case.scale, out,
+                                        case.rows_per_slot)
+    else:
+        fn = dsa.dsa_sparse_attn_decode if case.mode == "decode" else dsa.dsa_sparse_attn_prefill
+        fn(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], case.scale, out)
     code = dsa.dsa_get_device_error()
     host = buf.cpu().numpy().view(np.uint32)
     if check_guards:

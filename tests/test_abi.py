@@ -108,3 +108,16 @@ def test_topk_host_validation_before_any_launch(lib):
     assert call(k=2049, k_max=4096) == dsa.DSA_ERR_UNSUPPORTED
     assert call(ld=32772) == dsa.DSA_ERR_UNSUPPORTED
     assert call(R=0, scores=0) == dsa.DSA_OK
+
+
+def test_decode_rows_host_validation(lib):
+    def call(B=2, T=2, **kw):
+        a = dict(q=FAKE, kv=FAKE, idx=FAKE, n_sel=FAKE, sink=FAKE, out=FAKE)
+        a.update(kw)
+        return lib.dsa_sparse_attn_decode_rows(a["q"], a["kv"], a["idx"], a["n_sel"], a["sink"], 0.1,
+                                               a["out"], B, T, 64, 100, 8, dsa.DSA_BF16, None)
+    assert call(T=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(B=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert call(B=1 << 20, T=1 << 12) == dsa.DSA_ERR_INVALID_ARG     # rows beyond int range
+    assert call(q=0) == dsa.DSA_ERR_INVALID_ARG
+    assert call(B=0, q=0, out=0) == dsa.DSA_OK
