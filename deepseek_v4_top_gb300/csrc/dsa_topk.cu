@@ -51,7 +51,7 @@ __device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 21 : (
 __device__ __forceinline__ uint32_t digit_bins(int pass) { return pass == 2 ? 1024u : 2048u; }
 
 template <int kThreads, int kPerThread>
-__global__ void __launch_bounds__(kThreads, 1024 / kThreads) dsa_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 6 : 1)   // six short-row CTAs an SM dsa_topk_kernel(const TopkParams p) {
     using Smem = TopkSmem<kThreads>;
     constexpr int kWarps = Smem::kWarps;
     constexpr int kBinsPerThread = kTopkBins / kThreads;
