@@ -50,8 +50,9 @@ struct TopkSmem {
 __device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
 __device__ __forceinline__ uint32_t digit_bins(int pass) { return pass == 2 ? 1024u : 2048u; }
 
+// Short rows run six CTAs an SM (40 registers), long rows one.
 template <int kThreads, int kPerThread>
-__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 6 : 1)   // six short-row CTAs an SM dsa_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 6 : 1) dsa_topk_kernel(const TopkParams p) {
     using Smem = TopkSmem<kThreads>;
     constexpr int kWarps = Smem::kWarps;
     constexpr int kBinsPerThread = kTopkBins / kThreads;
