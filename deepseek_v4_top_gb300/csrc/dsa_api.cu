@@ -170,13 +170,11 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     const int chunks = decode ? (k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys : 1;
     p.chunk_keys = chunks > 1 ? kDecodeChunkKeys : k_max;
     p.chunks = chunks;
-    p.parts = R * chunks;
+    p.units = R * chunks;
     p.partial = chunks > 1 ? 1 : 0;
-    p.halves = column_halves(p.partial, p.parts, ds->sm_count);
-    p.units = p.parts * p.halves;
     if (p.partial) {
         const size_t bytes =
-            static_cast<size_t>(p.parts) * kPartialFloats * sizeof(float);
+            static_cast<size_t>(p.units) * kPartialFloats * sizeof(float);
         st = ensure_scratch(ds, bytes, &p.part);
         if (st != DSA_OK) return st;
     }
@@ -193,7 +191,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
         c.R = R;
         c.H = H;
         c.chunks = chunks;
-        c.units = p.parts;
+        c.units = p.units;
         if (launch_combine(c, s) != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;

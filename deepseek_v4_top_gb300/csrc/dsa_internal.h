@@ -12,10 +12,8 @@ constexpr int kTileKeys = 128;      // keys per tensor-core tile (MMA M)
 constexpr int kHeadsPad = 64;       // heads per tensor-core tile (MMA N)
 // Decode rows are split into key chunks of this size so that a small batch
 // still spreads over many SMs; each chunk leaves (m, l, O) partials that a
-// second kernel merges in chunk order.  The split (and the column halves)
-// depends only on the call's shape and how the output is divided, never on
-// the arithmetic of a partial, so a row's result does not depend on the
-// rest of the batch.
+// second kernel merges in chunk order.  It depends only on the call's shape,
+// so a row's result does not depend on the rest of the batch.
 constexpr int kDecodeChunkKeys = 128;
 // Floats of one chunk's partial result: O [64][512] plus (m, l) [2][64].
 constexpr size_t kPartialFloats = static_cast<size_t>(kHeadsPad) * kD + 2 * kHeadsPad;
@@ -31,7 +29,7 @@ struct TcParams {
     const int32_t* n_sel;     // [R]
     const float* sink;        // [H]
     float* out;               // final mode: [R][H][512]
-    float* part;              // partial mode: O [parts][64][512] then (m, l) [parts][2][64]
+    float* part;              // partial mode: O [units][64][512] then (m, l) [units][2][64]
     uint32_t* err;            // device error word
     int* queue;               // null: units round-robin over the grid; else the launch's unit
                               // queue [next ticket, CTAs finished], zero at launch, left zero
@@ -39,12 +37,8 @@ struct TcParams {
     int R, H, N, k_max;
     int decode;               // 0: prefill (one cache); T >= 1: row r reads slot r / T
     int chunk_keys;           // keys per unit (multiple of 16)
-    int chunks;               // key chunks per row
-    int halves;               // 1, or 2: each (row, chunk) runs as two units, one per column half
-                              // of the output (same gather, scores and softmax; half the P.V
-                              // and half the stores), when that still fits in one wave of CTAs
-    int parts;                // R * chunks: partial results (row, chunk)
-    int units;                // parts * halves
+    int chunks;               // units per row
+    int units;                // R * chunks
     int partial;              // 1: write partials instead of final outputs
 };
 
@@ -65,16 +59,8 @@ struct CombineParams {
     const float* part;        // as TcParams::part
     const float* sink;
     float* out;
-    int R, H, chunks, units;  // units: R * chunks partials
+    int R, H, chunks, units;
 };
-
-// Column halves for a launch of `parts` (row, key chunk) partials: a split
-// decode runs each partial as two units (each computes and stores half of
-// the output columns) when all of them still fit in one wave of CTAs.  The
-// partials are bit-identical either way.
-inline int column_halves(int partial, int parts, int sm_count) {
-    return partial && 2LL * parts <= sm_count ? 2 : 1;
-}
 
 // One launch of the top-k selection kernel (dsa_topk.cu).
 struct TopkParams {

@@ -115,10 +115,8 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
     p.decode = 1;
     p.chunks = static_cast<int>(chunks);
     p.chunk_keys = chunks > 1 ? kDecodeChunkKeys : k_max;
-    p.parts = B * p.chunks;
+    p.units = B * p.chunks;
     p.partial = chunks > 1 ? 1 : 0;
-    p.halves = column_halves(p.partial, p.parts, d->sm_count);
-    p.units = p.parts * p.halves;
     const int grid = p.units < d->sm_count ? p.units : d->sm_count;
     if (launch_tc(p, grid, s) != cudaSuccess) return DSA_ERR_CUDA;
     if (p.partial) {
@@ -129,7 +127,7 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
         c.R = B;
         c.H = H;
         c.chunks = p.chunks;
-        c.units = p.parts;
+        c.units = p.units;
         if (launch_combine(c, s) != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;

@@ -157,11 +157,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 __device__ __align__(16) uint32_t kNanRowBf16[256] = {DSA_R64(0x7FC07FC0u), DSA_R64(0x7FC07FC0u),
                                                       DSA_R64(0x7FC07FC0u), DSA_R64(0x7FC07FC0u)};
 
-// A unit: column half `half` (of kH, the launch's p.halves, a template
-// parameter of the kernel) of key chunk c of row r; its partial, when the row
-// is split, is number pu = r * p.chunks + c.
 struct Unit {
-    int r, c, pu, half, n_valid, tiles, bad_n;
+    int r, c, n_valid, tiles, bad_n;
 };
 
 // Whether every sink of the launch is finite (the same answer in every lane).
@@ -171,16 +168,10 @@ __device__ __forceinline__ bool sinks_finite(const TcParams& p, int lane) {
     return __all_sync(0xffffffffu, a && b);
 }
 
-template <int kH>
-__device__ __forceinline__ int row_of(const TcParams& p, int u) { return u / (p.chunks * kH); }
-
-template <int kH>
 __device__ __forceinline__ Unit unit_from(const TcParams& p, int u, int ns) {
     Unit x;
-    x.pu = u / kH;
-    x.half = u - x.pu * kH;
-    x.r = x.pu / p.chunks;
-    x.c = x.pu - x.r * p.chunks;
+    x.r = u / p.chunks;
+    x.c = u - x.r * p.chunks;
     x.bad_n = (ns < 0 || ns > p.k_max);
     const int eff = x.bad_n ? 1 : ns;                 // bad row: one NaN key
     int nv = eff - x.c * p.chunk_keys;
@@ -190,9 +181,8 @@ __device__ __forceinline__ Unit unit_from(const TcParams& p, int u, int ns) {
     return x;
 }
 
-template <int kH>
 __device__ __forceinline__ Unit unit_info(const TcParams& p, int u) {
-    return unit_from<kH>(p, u, __ldg(p.n_sel + row_of<kH>(p, u)));
+    return unit_from(p, u, __ldg(p.n_sel + u / p.chunks));
 }
 
 // The CTA's nu-th unit, or p.units when it has no more: round-robin over
@@ -266,10 +256,8 @@ __device__ __forceinline__ float warp_transpose_reduce32(float* v, int lane) {
 // n_sel) into shared memory with cp.async while the previous tile is being
 // computed, so that no thread holds them in registers meanwhile.  Entries at
 // or past k_max are never read.
-template <int kH>
 __device__ __forceinline__ void prefetch_idx(const TcParams& p, int u, int t, Misc& ms, int lane) {
-    const int pu = u / kH;
-    const int r = pu / p.chunks, c = pu - r * p.chunks;
+    const int r = u / p.chunks, c = u - r * p.chunks;
     const int* row = p.idx + static_cast<size_t>(r) * p.k_max;
     const int k0 = c * p.chunk_keys + t * 128;
 #pragma unroll
@@ -286,11 +274,14 @@ __device__ __forceinline__ void prefetch_idx(const TcParams& p, int u, int t, Mi
 // 32q + 32) of the tile: worker thread (warp w, lane l) copies 16 bytes
 // (column chunk l%8) of each 128-byte segment of row 4*(w + 8q) + l/8.  Keys
 // past n_valid are zero-filled, an out-of-range selection copies a NaN row.
-template <int q>
+// kShared: several decode rows share a slot (row r reads slot r / p.decode);
+// a separate kernel instance, so that the common one keeps its plain address.
+template <int q, bool kShared>
 __device__ __forceinline__ void issue_rows(const TcParams& p, const Misc& ms, const Unit& un, int t,
                                           uint32_t sKv, int wt) {
     const int w = wt >> 5, lane = wt & 31, cc = lane & 7;
-    const uint16_t* cache = p.kv + (p.decode ? static_cast<size_t>(un.r / p.decode) * p.N * kD : 0);
+    const size_t slot = kShared ? static_cast<size_t>(un.r / p.decode) : static_cast<size_t>(un.r);
+    const uint16_t* cache = p.kv + (p.decode ? slot * p.N * kD : 0);
     const uint16_t* nan_row = reinterpret_cast<const uint16_t*>(kNanRowBf16);
     {
         const int j = 4 * (w + 8 * q) + (lane >> 3);
@@ -321,10 +312,9 @@ __device__ __forceinline__ void score_mmas(uint32_t d, uint64_t dKv, uint64_t dQ
     score_mma_step<0>(d, dKv, dQ);
 }
 
-// O^T += V^T x P^T for 16 keys (k-step kk) of the 128-column chunks set in
-// cm (all four, or one column half's two): the stacked N=128 operand for
-// chunks 0-2, two N=64 operands for chunk 3.
-template <int kk, uint32_t cm>
+// O^T += V^T x P^T for 16 keys (k-step kk) of every 128-column chunk: the
+// stacked N=128 operand for chunks 0-2, two N=64 operands for chunk 3.
+template <int kk>
 __device__ __forceinline__ void pv_kstep(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi, uint64_t dPlo,
                                          uint32_t acc0) {
     constexpr uint32_t idPV128 = idesc_bf16(128, 128, true, true);
@@ -332,40 +322,26 @@ __device__ __forceinline__ void pv_kstep(uint32_t tmem, uint64_t dV, uint64_t dP
     constexpr uint32_t boff = (kk * 2048) >> 4;
     constexpr uint32_t a0 = (0 * kSegBytes + kk * 2048) >> 4, a1 = (2 * kSegBytes + kk * 2048) >> 4;
     constexpr uint32_t a2 = (4 * kSegBytes + kk * 2048) >> 4, a3 = (6 * kSegBytes + kk * 2048) >> 4;
-    if constexpr ((cm & 1u) != 0) umma_bf16_at<a0, boff>(tmem + tmem_o(0), dV, dPst, idPV128, acc0 | kk);
-    if constexpr ((cm & 2u) != 0) umma_bf16_at<a1, boff>(tmem + tmem_o(1), dV, dPst, idPV128, acc0 | kk);
-    if constexpr ((cm & 4u) != 0) umma_bf16_at<a2, boff>(tmem + tmem_o(2), dV, dPst, idPV128, acc0 | kk);
-    if constexpr ((cm & 8u) != 0) {
-        umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPhi, idPV64, acc0 | kk);
-        umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPlo, idPV64, 1u);
-    }
+    umma_bf16_at<a0, boff>(tmem + tmem_o(0), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a1, boff>(tmem + tmem_o(1), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a2, boff>(tmem + tmem_o(2), dV, dPst, idPV128, acc0 | kk);
+    umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPhi, idPV64, acc0 | kk);
+    umma_bf16_at<a3, boff>(tmem + tmem_o(3), dV, dPlo, idPV64, 1u);
 }
 
 // Keys [32q, 32q + 32) of the tile, then a commit that frees those rows of
 // the KV buffer for the next tile's gather.
 // The last quarter is released in two halves, so only 16 rows are left to
 // gather once the P.V is over.
-template <int q, uint32_t cm>
+template <int q>
 __device__ __forceinline__ void pv_quarter(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi,
                                            uint64_t dPlo, uint32_t acc0, Misc& ms) {
-    pv_kstep<2 * q, cm>(tmem, dV, dPst, dPhi, dPlo, acc0);
+    pv_kstep<2 * q>(tmem, dV, dPst, dPhi, dPlo, acc0);
     if (q == 3) umma_commit(smem_addr(&ms.kv_free[3]));
-    pv_kstep<2 * q + 1, cm>(tmem, dV, dPst, dPhi, dPlo, acc0);
+    pv_kstep<2 * q + 1>(tmem, dV, dPst, dPhi, dPlo, acc0);
     umma_commit(smem_addr(&ms.kv_free[q == 3 ? 4 : q]));
 }
 
-// The P.V of one tile for the output chunks in cm, one straight-line issue
-// sequence per chunk set.
-template <uint32_t cm>
-__device__ __forceinline__ void pv_tile(uint32_t tmem, uint64_t dV, uint64_t dPst, uint64_t dPhi, uint64_t dPlo,
-                                        uint32_t acc0, Misc& ms) {
-    pv_quarter<0, cm>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-    pv_quarter<1, cm>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-    pv_quarter<2, cm>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-    pv_quarter<3, cm>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-}
-
-template <int kH>
 __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem, bool sinks) {
     const uint32_t sKv = smem_addr(smem + kOffKv);
     const uint32_t sQ = smem_addr(smem + kOffQ);
@@ -387,7 +363,7 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
     for (;; ++nu) {
         const int u = unit_at(p, ms, nu);
         if (u >= p.units) break;
-        const Unit un = unit_info<kH>(p, u);
+        const Unit un = unit_info(p, u);
         if (!mbar_wait(smem_addr(&ms.q_full), nu & 1, ab, p.err)) return;
         for (int t = 0; t < un.tiles; ++t, ++g) {
             // scores: S^T[key][head] over the 512 columns, 16 at a time
@@ -424,13 +400,10 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
             if (t == 0 && nu > 0 && !mbar_wait(smem_addr(&ms.o_free), (nu - 1) & 1, ab, p.err)) return;
             tc_fence_after();
             const uint32_t acc0 = t > 0 ? 1u : 0u;
-            if constexpr (kH == 1) {
-                pv_tile<0xFu>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-            } else if (un.half == 0) {
-                pv_tile<0x3u>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-            } else {
-                pv_tile<0xCu>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
-            }
+            pv_quarter<0>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<1>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<2>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
+            pv_quarter<3>(tmem, dV, dPst, dPhi, dPlo, acc0, ms);
             if (t == un.tiles - 1) umma_commit(smem_addr(&ms.o_full));
         }
     }
@@ -688,7 +661,7 @@ __device__ __forceinline__ bool softmax_tile(const TcParams& p, uint8_t* smem, M
     return true;
 }
 
-template <int kH>
+template <bool kShared>
 __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tmem) {
     WorkerCtx c;
     c.wt = threadIdx.x;
@@ -715,22 +688,21 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
         // 1-2. gather this tile, 32 keys at a time, each as soon as the previous
         //      tile's P.V is done with those rows of the buffer
         if (!mbar_wait(smem_addr(&ms.idx_full), g & 1, ab, p.err)) return;
-        if (t == 0) un = unit_from<kH>(p, u, ms.idx_nsel);
-        if (t == 0 && un.bad_n && un.pu % p.chunks == 0 && un.half == 0 && c.wt == 0)
-            atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
+        if (t == 0) un = unit_from(p, u, ms.idx_nsel);
+        if (t == 0 && un.bad_n && un.c == 0 && c.wt == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
         const uint32_t ph = (g - 1) & 1;
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[0]), ph, ab, p.err)) return;
-        issue_rows<0>(p, ms, un, t, sKv, c.wt);
+        issue_rows<0, kShared>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[1]), ph, ab, p.err)) return;
-        issue_rows<1>(p, ms, un, t, sKv, c.wt);
+        issue_rows<1, kShared>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[2]), ph, ab, p.err)) return;
-        issue_rows<2>(p, ms, un, t, sKv, c.wt);
+        issue_rows<2, kShared>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
         // rows 96-111 (warps 0-3) are free one k-step before rows 112-127
         if (g > 0 && !mbar_wait(smem_addr(&ms.kv_free[c.w < 4 ? 3 : 4]), ph, ab, p.err)) return;
-        issue_rows<3>(p, ms, un, t, sKv, c.wt);
+        issue_rows<3, kShared>(p, ms, un, t, sKv, c.wt);
         cp_async_arrive(smem_addr(&ms.kv_full));
         if (t == 0 && c.sinks) {
             // the unit starts from the sink references
@@ -769,15 +741,14 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
 // A spare warp walks the same tiles as the workers and copies the indices of
 // tile g + 1 as soon as the scores of tile g are ready (by then every worker
 // has issued tile g's gather, so idx[] is free).
-template <int kH>
 __device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
     volatile int* ab = &ms.abort_flag;
     // with a launch queue this warp takes the CTA's units, one unit ahead
     int u = p.queue ? take_unit(p, ms, 0, lane) : static_cast<int>(blockIdx.x);
     if (u >= p.units) return;
     int u_next = p.queue ? take_unit(p, ms, 1, lane) : u + static_cast<int>(gridDim.x);
-    prefetch_idx<kH>(p, u, 0, ms, lane);
-    Unit un = unit_info<kH>(p, u);
+    prefetch_idx(p, u, 0, ms, lane);
+    Unit un = unit_info(p, u);
     int t = 0, g = 0, nu = 0;
     while (true) {
         int u2 = u, t2 = t + 1;
@@ -787,11 +758,11 @@ __device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
         }
         if (u2 >= p.units) break;
         if (!mbar_wait(smem_addr(&ms.s_full), g & 1, ab, p.err)) break;
-        prefetch_idx<kH>(p, u2, t2, ms, lane);
+        prefetch_idx(p, u2, t2, ms, lane);
         if (t2 == 0) {
             u = u2;
             ++nu;
-            un = unit_info<kH>(p, u);
+            un = unit_info(p, u);
             u_next = p.queue ? take_unit(p, ms, nu + 1, lane) : u + static_cast<int>(gridDim.x);
         }
         t = t2;
@@ -804,7 +775,6 @@ __device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
 // One thread of a spare warp: loads each unit's Q by tiled TMA as soon as
 // the last score MMA of the unit before has read the buffer, off the
 // workers' path.
-template <int kH>
 __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
     volatile int* ab = &ms.abort_flag;
     const uint32_t sQ = smem_addr(smem + kOffQ);
@@ -816,7 +786,7 @@ __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
         if (u >= p.units) break;
         if (nu > 0 && !mbar_wait(smem_addr(&ms.q_free), (nu - 1) & 1, ab, p.err)) break;
         mbar_arrive_expect_tx(bar, q_bytes);
-        for (int s = 0; s < 8; ++s) tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, row_of<kH>(p, u) * p.H, bar);
+        for (int s = 0; s < 8; ++s) tma_load_2d(sQ + s * kQSegBytes, &p.tmap_q, s * 64, (u / p.chunks) * p.H, bar);
     }
     if (nu > 0) {
         // the copies armed here have landed before the CTA can exit
@@ -831,14 +801,12 @@ __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
 // then O^T read back 16 heads at a time, scaled and stored.  The stores take
 // about 4k cycles per unit (the SM writes ~32 bytes a clock); overlapped
 // with the next unit's gather, scores and softmax they leave its chain.
-template <int kH>
 __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, int lane) {
     volatile int* ab = &ms.abort_flag;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     for (int nu = 0;; ++nu) {
         const int u = unit_at(p, ms, nu);
         if (u >= p.units) break;
-        const int pu = u / kH, half = u - pu * kH;
         if (!mbar_wait(smem_addr(&ms.l_ready), nu & 1, ab, p.err)) return;
         float f[2];     // heads lane and lane + 32
 #pragma unroll
@@ -854,9 +822,9 @@ __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, 
                 const float e1 = exp2f(mu - mstar);
                 const float e2 = exp2f(s2 - mstar);
                 f[e] = e1 / (l * e1 + e2);
-            } else if (qd == 0 && half == 0) {
-                float* ml = p.part + static_cast<size_t>(p.parts) * kHeadsPad * kD +
-                            static_cast<size_t>(pu) * 2 * kHeadsPad;
+            } else if (qd == 0) {
+                float* ml = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD +
+                            static_cast<size_t>(u) * 2 * kHeadsPad;
                 ml[h] = m;
                 ml[kHeadsPad + h] = l;
             }
@@ -865,17 +833,16 @@ __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, 
         if (lane == 0) mbar_arrive(smem_addr(&ms.l_free));
         if (!mbar_wait(smem_addr(&ms.o_full), nu & 1, ab, p.err)) return;
         tc_fence_after();
-        float* dst = p.partial ? p.part + static_cast<size_t>(pu) * kHeadsPad * kD
-                               : p.out + static_cast<size_t>(row_of<kH>(p, u)) * p.H * kD;
+        float* dst = p.partial ? p.part + static_cast<size_t>(u) * kHeadsPad * kD
+                               : p.out + static_cast<size_t>(u / p.chunks) * p.H * kD;
         const int d0 = 32 * qd + lane;
-        const int i0 = half * (4 / kH), i1 = i0 + 4 / kH;     // this unit's chunks
 #pragma unroll 1
         for (int hg = 0; hg < 4; ++hg) {
             float fh[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) fh[j] = __shfl_sync(0xffffffffu, hg < 2 ? f[0] : f[1], 16 * (hg & 1) + j);
 #pragma unroll 1
-            for (int i = i0; i < i1; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 // chunks 0-2 keep the hi and lo halves 64 columns apart
                 const uint32_t ta = tmem + lane_off + tmem_o(i) + 16 * hg;
                 float o[16];
@@ -900,7 +867,7 @@ __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, 
     }
 }
 
-template <int kH>
+template <bool kShared>
 __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -958,21 +925,21 @@ __global__ void __launch_bounds__(kThreads, 1) dsa_tc_kernel(const __grid_consta
 
     if (warp < kWorkerWarps) {
         regs_inc<kRegsWorker>();
-        worker_role<kH>(p, smem, ms, tmem);
+        worker_role<kShared>(p, smem, ms, tmem);
         cp_async_wait_all();
         __syncwarp();
     } else if (warp < kOutWarp0 + kOutWarps) {
         regs_dec<kRegsOther>();
-        output_role<kH>(p, ms, tmem, warp & 3, threadIdx.x & 31);
+        output_role(p, ms, tmem, warp & 3, threadIdx.x & 31);
         __syncwarp();
     } else {
         regs_dec<kRegsOther>();
-        if (warp == kQWarp && (threadIdx.x & 31) == 0) q_role<kH>(p, smem, ms);
-        if (warp == kIdxWarp) idx_role<kH>(p, ms, threadIdx.x & 31);
+        if (warp == kQWarp && (threadIdx.x & 31) == 0) q_role(p, smem, ms);
+        if (warp == kIdxWarp) idx_role(p, ms, threadIdx.x & 31);
         // the whole warp tests the sinks, one thread issues
         const bool sinks = warp == kMmaWarp && sinks_finite(p, threadIdx.x & 31);
         if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
-            mma_role<kH>(p, smem, ms, tmem, sinks);
+            mma_role(p, smem, ms, tmem, sinks);
             // every MMA this thread issued has completed before TMEM is freed
             umma_commit(smem_addr(&ms.drain));
             int dummy = 0;
@@ -1048,10 +1015,10 @@ cudaError_t launch_tc(const TcParams& params, int grid, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(g_launch_mu);
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(dsa_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(dsa_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes));
             if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(dsa_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(dsa_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes));
             if (e != cudaSuccess) return e;
             attr_set[dev] = true;
@@ -1073,9 +1040,8 @@ cudaError_t launch_tc(const TcParams& params, int grid, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.halves == 2) return cudaLaunchKernelEx(&cfg, dsa_tc_kernel<2>, p);
-    if (p.halves != 1) return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, dsa_tc_kernel<1>, p);
+    return p.decode > 1 ? cudaLaunchKernelEx(&cfg, dsa_tc_kernel<true>, p)
+                        : cudaLaunchKernelEx(&cfg, dsa_tc_kernel<false>, p);
 }
 
 }  // namespace dsa

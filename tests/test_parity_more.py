@@ -124,11 +124,10 @@ def test_scores_far_above_the_sinks(mode):
 
 
 def test_decode_rows_match_across_combine_paths():
-    # 40 rows x 5 chunks = 200 partials: more units than SMs, so the chunks
-    # merge through the scratch and the combine kernel.  The first 20 rows
-    # alone (100 units, one wave) merge on chip in thread-block clusters, and
-    # the first 5 rows alone do too, each (row, chunk) split in two column
-    # halves.  A row must give the same bits on every path.
+    # 40 rows x 5 chunks = 200 units: more than SMs, so CTAs run several
+    # units and the combine merges partials written in different rounds.  The
+    # first 20 rows alone (100 units) and the first 5 alone (25 units) run one
+    # unit a CTA.  A row must give the same bits in every launch.
     rng = np.random.default_rng(4700)
     big = I._edge_base(rng, "decode_b40", I.BF16, 64, 640, "decode", R=40, N=2048, k_extra=0)
     full, code = run(big)
