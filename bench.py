@@ -280,6 +280,28 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
     return sum(ms) / reps, c.R
 
 
+def bench_topk(args, world, rank, local):
+    """The top-k selection alone (for profiling): prints one JSON line with
+    the prefill-row and decode-row timings that the default run reports."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    pk, _ = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    out = {}
+    for mode in ("prefill", "decode"):
+        t_ms, rows, nbytes = topk_timing(dsa, dev, flush, mode, reps=max(1, args.steps))
+        out[mode] = {"ms": t_ms, "rows_per_s": rows / (t_ms * 1e-3),
+                     "scores_frac_hbm": nbytes / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    if rank == 0:
+        print(json.dumps({"metric": "top-k selection (k=%d), ms per call" % K, "workloads": out}), flush=True)
+
+
 def bench_ours(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
@@ -609,14 +631,17 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("both", "prefill", "decode"), default="both",
-                    help="both (the benchmark step) or one half of it, for profiling")
+    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk"), default="both",
+                    help="both (the benchmark step), one half of it for profiling, or the top-k "
+                         "selection alone")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
     if args.impl == "reference":
         bench_reference(args, world, rank)
+    elif args.workload == "topk":
+        bench_topk(args, world, rank, local)
     else:
         bench_ours(args, world, rank, local)
 
