@@ -225,6 +225,15 @@ def decode_sustained(dsa, d, case, dev):
     return e0.elapsed_time(e1) / (reps * SUS_CALLS)
 
 
+def hold_gpu(stream, ms=2.0):
+    """Keep the stream busy for about `ms` milliseconds, so that the host has
+    enqueued the timed calls that follow before the GPU reaches them: the
+    events then time the calls, not the host's launch latency."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 2.0e6))      # cycles at about 2 GHz
+
+
 def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
     """Mean milliseconds of one top-k selection call over the indexer-score
     rows of `mode` (prefill: 2048 causal rows of a 4096 cache; decode: 8
@@ -241,15 +250,15 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
     for _ in range(3):
         dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
     torch.cuda.synchronize()
-    ms = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    hold_gpu(stream)
     for i in range(reps):
         flush.fill_(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        ev[i][0].record(stream)
         dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     assert dsa.dsa_get_device_error() == 0
     return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
 
@@ -267,15 +276,15 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
     for _ in range(3):
         dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
     torch.cuda.synchronize()
-    ms = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    hold_gpu(stream)
     for i in range(reps):
         flush.fill_(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        ev[i][0].record(stream)
         dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     assert dsa.dsa_get_device_error() == 0
     return sum(ms) / reps, c.R
 
@@ -359,6 +368,7 @@ def bench_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    hold_gpu(stream)
     for i in range(args.steps):
         flush.fill_(float(i))            # evict L2 between steps (outside the events)
         ev[i][0].record(stream)

@@ -22,6 +22,8 @@ struct DeviceState {
     uint32_t* err = nullptr;       // error word, followed by the stream queues
     float* scratch = nullptr;
     size_t scratch_bytes = 0;
+    void* topk_scratch = nullptr;  // two-step top-k: the shares' picks
+    size_t topk_scratch_bytes = 0;
     int sm_count = 0;
     cudaStream_t queue_stream[kQueues] = {};
     int queues_used = 0;
@@ -58,25 +60,33 @@ dsa_status device_state(DeviceState** out) {
     return DSA_OK;
 }
 
-// Grows the decode scratch to `bytes` and returns it (under the lock, so a
+// Grows a scratch buffer to `bytes` and returns it (under the lock, so a
 // concurrent grow cannot free it between the check and the use).
-dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
+dsa_status ensure_buffer(void** buf, size_t* have, size_t bytes, void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (st->scratch_bytes >= bytes) {
-        *out = st->scratch;
+    if (*have >= bytes) {
+        *out = *buf;
         return DSA_OK;
     }
-    if (st->scratch) {
+    if (*buf) {
         // the old buffer may still be read by queued work
         if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
-        cudaFree(st->scratch);
-        st->scratch = nullptr;
-        st->scratch_bytes = 0;
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
     }
-    if (cudaMalloc(&st->scratch, bytes) != cudaSuccess) return DSA_ERR_CUDA;
-    st->scratch_bytes = bytes;
-    *out = st->scratch;
+    if (cudaMalloc(buf, bytes) != cudaSuccess) return DSA_ERR_CUDA;
+    *have = bytes;
+    *out = *buf;
     return DSA_OK;
+}
+
+// The decode scratch.
+dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
+    void* v = nullptr;
+    const dsa_status r = ensure_buffer(reinterpret_cast<void**>(&st->scratch), &st->scratch_bytes, bytes, &v);
+    *out = static_cast<float*>(v);
+    return r;
 }
 
 // The row queue of stream s, or null (round-robin rows) when s may run on
@@ -242,8 +252,36 @@ dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, 
     p.ld = ld;
     p.k = k;
     p.k_max = k_max;
-    const int grid = R < (1 << 20) ? R : (1 << 20);
-    return dsa::launch_topk(p, grid, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    p.shares = dsa::topk_shares(ld);
+    p.cand_ld = (p.shares * k + 3) & ~3;
+    p.cand_key = nullptr;
+    p.cand_pos = nullptr;
+    // long rows go in two steps through a scratch of at most 256 MB: as many
+    // rows at a time as fit
+    int rows = R;
+    if (p.shares > 1) {
+        const size_t row_bytes = static_cast<size_t>(p.cand_ld) * 8;
+        const size_t fit = (static_cast<size_t>(256) << 20) / row_bytes;
+        rows = fit < static_cast<size_t>(R) ? static_cast<int>(fit) : R;
+        rows = rows < (1 << 24) ? rows : (1 << 24);      // (rows x shares stays an int)
+        const size_t per = static_cast<size_t>(rows) * static_cast<size_t>(p.cand_ld);
+        void* buf = nullptr;
+        st = dsa::ensure_buffer(&ds->topk_scratch, &ds->topk_scratch_bytes, per * 8, &buf);
+        if (st != DSA_OK) return st;
+        p.cand_key = static_cast<uint32_t*>(buf);
+        p.cand_pos = reinterpret_cast<int32_t*>(p.cand_key + per);
+    }
+    for (int r0 = 0; r0 < R; r0 += rows) {
+        dsa::TopkParams q = p;
+        q.R = R - r0 < rows ? R - r0 : rows;
+        q.scores = scores + static_cast<size_t>(r0) * ld;
+        q.n_valid = n_valid + r0;
+        q.idx = idx + static_cast<size_t>(r0) * k_max;
+        q.n_sel = n_sel + r0;
+        const int grid = q.R < (1 << 20) ? q.R : (1 << 20);
+        if (dsa::launch_topk(q, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
 }
 
 dsa_status dsa_selftest_wait_limit(void* stream) {
@@ -286,13 +324,14 @@ dsa_status dsa_shutdown(void) {
     dsa_status st = DSA_OK;
     for (int d = 0; d < dsa::kMaxDevices; ++d) {
         dsa::DeviceState& ds = dsa::g_dev[d];
-        if (!ds.err && !ds.scratch) continue;
+        if (!ds.err && !ds.scratch && !ds.topk_scratch) continue;
         if (cudaSetDevice(d) != cudaSuccess) {
             st = DSA_ERR_CUDA;
             continue;
         }
         if (ds.err) cudaFree(ds.err);
         if (ds.scratch) cudaFree(ds.scratch);
+        if (ds.topk_scratch) cudaFree(ds.topk_scratch);
         ds = dsa::DeviceState();
     }
     if (have_cur) cudaSetDevice(cur);

@@ -70,12 +70,19 @@ struct TopkParams {
     int32_t* n_sel;           // [R]
     uint32_t* err;            // device error word
     int R, ld, k, k_max;
+    // rows longer than one share (4096 positions) are selected in two steps
+    // through a scratch of [R][cand_ld] keys and positions: the picks of the
+    // row's `shares` shares, k each, share after share
+    int shares;               // topk_shares(ld)
+    int cand_ld;              // >= shares * k, a multiple of 4
+    uint32_t* cand_key;
+    int32_t* cand_pos;
 };
 
-// Largest k and row length the top-k kernel takes (a row's keys are held in
-// the registers of one CTA).
+// Largest k and row length the top-k kernel takes.
 constexpr int kTopkMaxK = 2048;
 constexpr int kTopkMaxLd = 32768;
+int topk_shares(int ld);
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t s);
 
 // Shared memory of the tensor-core kernel (bytes, dynamic).

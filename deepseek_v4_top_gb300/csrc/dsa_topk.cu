@@ -5,19 +5,36 @@
 // number, -0 equal to +0, equal scores by smaller position first; a row
 // keeps min(k, n_valid) positions in that order and pads with -1.
 //
-// One CTA a row (256 threads for rows of up to 4096 candidates, 1024 up to
-// 32768), the row's keys held in registers: warp w owns a contiguous share
-// of the positions, lane l positions share_w + l + 32 i.
+// A CTA selects over one segment of up to 16 keys a thread, held in
+// registers; thread t owns the segment's contiguous entries [16 t, 16 t + 16).
+// A row of up to 4096 positions is one segment, read as float4 (rows are
+// 16-byte aligned with a stride of a multiple of 4 scores).  A longer row is
+// selected in two steps: each 4096-position share of it selects its own top
+// k (one CTA a share, all the row's shares at once), and one CTA then selects
+// the row's top k among the shares' picks.  That is exact: a pick of the row
+// has fewer than k entries above it in the row, so fewer in its share.  The
+// shares' picks are stored share after share, each in position order, so the
+// second step sees them in position order too.
+// For a segment:
 //   1. the scores become 32-bit keys whose unsigned order is the selection
-//      order of the values (NaN lowest);
-//   2. a 3-pass radix select (11, 11 and 10 bits, most significant first;
-//      2048-bin shared histograms, a block scan to find the bin) finds the
+//      order of the values (NaN lowest); entries past the segment get key 0;
+//   2. a radix select (11, 11 and 10 bits, most significant first) finds the
 //      key T of the k-th pick and how many keys equal to T it takes (the
-//      first ones by position);
-//   3. each warp counts the picks of its share, one prefix over the warps
-//      gives every share its output offset, and each warp writes its picks'
-//      positions in ascending order.
-// The picks depend only on the row, never on the launch.
+//      first ones by position).  Each pass counts into a 2048-bin shared
+//      histogram whose bins, counted from the top, are owned B to a thread
+//      (their addresses padded so that a warp reading the b-th bin of each
+//      thread hits 32 banks); a scan of the owners' sums finds the bin that
+//      holds the k-th pick.  A pass whose bin is taken whole ends the select
+//      early (a row of N(0,1) scores usually ends after two passes);
+//   3. one block scan of packed per-thread counts (keys above T in the high
+//      16 bits, keys equal to T in the low) gives every thread its output
+//      offset, the keys above T before it plus min(keys equal to T before
+//      it, need), and each thread writes its own picks in position order.
+// Entries past the segment hold key 0, the key of NaN, and come after every
+// candidate: they can only fall in the lowest bin of a pass, whose count then
+// exceeds the candidates' but never changes which bin is chosen, and they are
+// never among the first `need` keys equal to T.  The picks depend only on the
+// row, never on the launch.
 #include <stdint.h>
 
 #include "dsa_internal.h"
@@ -27,45 +44,75 @@ namespace dsa {
 namespace {
 
 constexpr int kTopkBins = 2048;
+constexpr int kTopkPerThread = 16;
+constexpr int kTopkShare = 256 * kTopkPerThread;     // positions a share (and a one-step row) holds
 
-// Order-preserving key of a score: NaN -> 0, -0 -> the key of +0, negative
-// values bit-inverted, positive values with the sign bit set.
+// What a launch selects over and where it writes.
+enum TopkMode {
+    kRowsToIdx = 0,      // rows of up to 4096 scores -> idx, n_sel
+    kSharesToCand = 1,   // a share of a long row -> its picks' keys and positions
+    kCandToIdx = 2,      // a long row's shares' picks -> idx, n_sel
+};
+
+// Order-preserving key of a score: NaN -> 0; otherwise positive values with
+// the sign bit set and negative values negated (two's complement), which
+// sends -0 and +0 to the same key 0x80000000.
 __device__ __forceinline__ uint32_t score_key(float x) {
-    uint32_t u = __float_as_uint(x);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
-    if (u == 0x80000000u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t s = static_cast<uint32_t>(static_cast<int32_t>(u) >> 31);
+    const uint32_t k = (u ^ (s | 0x80000000u)) - s;
+    return x == x ? k : 0u;
 }
 
 template <int kThreads>
 struct TopkSmem {
     static constexpr int kWarps = kThreads / 32;
-    uint32_t hist[kTopkBins];
-    uint32_t warp_sum[kWarps];      // bin-scan totals, then per-share counts above T
-    uint32_t warp_eq[kWarps];       // per share: keys equal to T
-    uint32_t prefix, need;          // radix select state: key bits fixed so far, picks left
+    static constexpr int kBinsPerThread = kTopkBins / kThreads;
+    // one padding word after every kBinsPerThread bins
+    static constexpr int kSlots = kTopkBins + kTopkBins / kBinsPerThread;
+    uint32_t hist[kSlots];
+    uint32_t warp_sum[kWarps];
+    uint32_t prefix, need, done;    // select state: key bits fixed so far, picks left, bin taken whole
 };
+
+template <int kBinsPerThread>
+__device__ __forceinline__ int bin_slot(uint32_t d) { return static_cast<int>(d + d / kBinsPerThread); }
 
 // The digit passes: bits [21, 32), [10, 21), [0, 10).
 __device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
-__device__ __forceinline__ uint32_t digit_bins(int pass) { return pass == 2 ? 1024u : 2048u; }
+__device__ __forceinline__ int digit_bins(int pass) { return pass == 2 ? 1024 : 2048; }
 
-// Short rows run six CTAs an SM (40 registers), long rows one.
-template <int kThreads, int kPerThread>
-__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 6 : 1) dsa_topk_kernel(const TopkParams p) {
+// Picks a long row's shares hold before share c: k for every earlier share
+// (a share that holds candidates has only full shares before it).
+__device__ __forceinline__ int share_len(int n, int c) {
+    const int len = n - c * kTopkShare;
+    return len < 0 ? 0 : (len > kTopkShare ? kTopkShare : len);
+}
+
+template <int kThreads, int kMode>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 4 : 1) dsa_topk_kernel(const TopkParams p) {
     using Smem = TopkSmem<kThreads>;
     constexpr int kWarps = Smem::kWarps;
-    constexpr int kBinsPerThread = kTopkBins / kThreads;
+    constexpr int kB = Smem::kBinsPerThread;
+    static_assert(kB >= 2 && kThreads * kB == kTopkBins, "bin ownership");
     __shared__ Smem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t lt_mask = (1u << lane) - 1u;
     grid_launch_dependents();
     grid_dependency_wait();          // the scores may come from the grid before this one
+#pragma unroll
+    for (int b = 0; b < kB; ++b) sm.hist[bin_slot<kB>(tid * kB + b)] = 0u;
 
-    for (int r = blockIdx.x; r < p.R; r += gridDim.x) {
+    const int segments = kMode == kSharesToCand ? p.R * p.shares : p.R;
+    for (int sg = blockIdx.x; sg < segments; sg += gridDim.x) {
+        const int r = kMode == kSharesToCand ? sg / p.shares : sg;
+        const int c = kMode == kSharesToCand ? sg - r * p.shares : 0;
         const int n = __ldg(p.n_valid + r);
+        const bool bad = n < 0 || n > p.ld;
         int32_t* out = p.idx + static_cast<size_t>(r) * p.k_max;
-        if (n < 0 || n > p.ld) {
+        uint32_t* cand_key = p.cand_key + static_cast<size_t>(r) * p.cand_ld;
+        int32_t* cand_pos = p.cand_pos + static_cast<size_t>(r) * p.cand_ld;
+        if (kMode == kSharesToCand && bad) continue;       // (the second step reports the row)
+        if (kMode != kSharesToCand && bad) {
             if (tid == 0) {
                 atomicOr(p.err, DSA_DEVERR_NVALID_RANGE);
                 p.n_sel[r] = 0;
@@ -73,137 +120,224 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 6 : 1) dsa_topk_ke
             for (int j = tid; j < p.k_max; j += kThreads) out[j] = -1;
             continue;
         }
-        const int m = n < p.k ? n : p.k;
-        // 1. keys of this thread's positions (coalesced per warp)
-        const int share = (n + kWarps * 32 - 1) / (kWarps * 32) * 32;
-        const int j_lo = warp * share, j_hi = min(n, j_lo + share);
-        const float* row = p.scores + static_cast<size_t>(r) * p.ld;
-        uint32_t key[kPerThread];
+        // the segment: n_seg entries; its picks, m, go to offset `at0` of the output
+        int n_seg, m;
+        if (kMode == kRowsToIdx) {
+            n_seg = n;
+            m = n < p.k ? n : p.k;
+        } else if (kMode == kSharesToCand) {
+            n_seg = share_len(n, c);
+            m = n_seg < p.k ? n_seg : p.k;
+            if (n_seg == 0) continue;
+        } else {
+            const int full = n / kTopkShare, part = n - full * kTopkShare;
+            n_seg = full * p.k + (part < p.k ? part : p.k);
+            m = n < p.k ? n : p.k;
+        }
+        const int share0 = c * kTopkShare;                  // first position of the share
+        const int at0 = c * p.k;                            // its picks' offset among the row's
+        if (kMode != kSharesToCand && m == n_seg) {
+            // every entry is a pick, in position order
+            for (int j = tid; j < p.k_max; j += kThreads)
+                out[j] = j < n_seg ? (kMode == kCandToIdx ? cand_pos[j] : j) : -1;
+            if (tid == 0) p.n_sel[r] = m;
+            continue;
+        }
+
+        // 1. keys of this thread's entries
+        const int j0 = tid * kTopkPerThread;
+        const int rem = n_seg - j0;  // this thread's entries: the first min(max(rem, 0), 16)
+        uint32_t key[kTopkPerThread];
+        if (kMode == kCandToIdx) {
+            const uint4* src4 = reinterpret_cast<const uint4*>(cand_key) + j0 / 4;
 #pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int j = j_lo + lane + 32 * i;
-            key[i] = j < j_hi ? score_key(__ldg(row + j)) : 0u;
+            for (int i = 0; i < kTopkPerThread / 4; ++i) {
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (4 * i < rem) v = src4[i];
+                key[4 * i] = 4 * i < rem ? v.x : 0u;
+                key[4 * i + 1] = 4 * i + 1 < rem ? v.y : 0u;
+                key[4 * i + 2] = 4 * i + 2 < rem ? v.z : 0u;
+                key[4 * i + 3] = 4 * i + 3 < rem ? v.w : 0u;
+            }
+        } else {
+            const float4* src4 =
+                reinterpret_cast<const float4*>(p.scores + static_cast<size_t>(r) * p.ld + share0) + j0 / 4;
+#pragma unroll
+            for (int i = 0; i < kTopkPerThread / 4; ++i) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (4 * i < rem) v = __ldg(src4 + i);
+                key[4 * i] = 4 * i < rem ? score_key(v.x) : 0u;
+                key[4 * i + 1] = 4 * i + 1 < rem ? score_key(v.y) : 0u;
+                key[4 * i + 2] = 4 * i + 2 < rem ? score_key(v.z) : 0u;
+                key[4 * i + 3] = 4 * i + 3 < rem ? score_key(v.w) : 0u;
+            }
+        }
+        if (kMode == kSharesToCand && m == n_seg) {
+            // a short share: all of it, in position order
+#pragma unroll
+            for (int i = 0; i < kTopkPerThread; ++i) {
+                if (i < rem) {
+                    cand_key[at0 + j0 + i] = key[i];
+                    cand_pos[at0 + j0 + i] = share0 + j0 + i;
+                }
+            }
+            continue;
         }
         if (tid == 0) {
             sm.prefix = 0u;
             sm.need = static_cast<uint32_t>(m);
+            sm.done = 0u;
         }
+        __syncthreads();             // (the histogram is clear: each pass clears it)
 
-        // 2. radix select of the m-th largest key (unless every candidate is a pick)
-        uint32_t thr = 0u, need = 0u;     // picks: keys > thr, and the first `need` keys == thr
-        const bool all = m == n;
-        if (!all) {
-            uint32_t mask = 0u;
-            for (int pass = 0; pass < 3; ++pass) {
-                const int shift = digit_shift(pass);
-                const uint32_t nb = digit_bins(pass);
+        // 2. radix select of the m-th largest key
 #pragma unroll
-                for (int b = 0; b < kBinsPerThread; ++b) sm.hist[tid * kBinsPerThread + b] = 0u;
-                __syncthreads();
-                const uint32_t prefix = sm.prefix;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = digit_shift(pass), nb = digit_bins(pass);
+            const int hi = shift + (pass == 2 ? 10 : 11);      // bits fixed before this pass: [hi, 32)
+            const uint32_t prefix = sm.prefix;
 #pragma unroll
-                for (int i = 0; i < kPerThread; ++i) {
-                    const int j = j_lo + lane + 32 * i;
-                    if (j < j_hi && (key[i] & mask) == prefix) atomicAdd(&sm.hist[(key[i] >> shift) & (nb - 1)], 1u);
-                }
-                __syncthreads();
-                // thread t holds bins counted from the top: nb-1-t*B .. nb-B-t*B
-                uint32_t c[kBinsPerThread], s = 0u;
-#pragma unroll
-                for (int b = 0; b < kBinsPerThread; ++b) {
-                    const int bin = static_cast<int>(nb) - 1 - tid * kBinsPerThread - b;
-                    c[b] = bin >= 0 ? sm.hist[bin] : 0u;
-                    s += c[b];
-                }
-                uint32_t incl = s;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                if (lane == 31) sm.warp_sum[warp] = incl;
-                const uint32_t want = sm.need;
-                __syncthreads();
-                uint32_t before = 0u;
-                for (int w = 0; w < warp; ++w) before += sm.warp_sum[w];
-                const uint32_t excl = before + incl - s;
-                if (excl < want && want <= excl + s) {
-                    uint32_t above = excl;
-#pragma unroll
-                    for (int b = 0; b < kBinsPerThread; ++b) {
-                        if (above + c[b] >= want) {
-                            const uint32_t bin = nb - 1u - tid * kBinsPerThread - b;
-                            sm.prefix = prefix | (bin << shift);
-                            sm.need = want - above;
-                            break;
-                        }
-                        above += c[b];
-                    }
-                }
-                mask |= (nb - 1u) << shift;
-                __syncthreads();
+            for (int i = 0; i < kTopkPerThread; ++i) {
+                if (pass == 0 || (key[i] >> hi) == (prefix >> hi))
+                    atomicAdd(&sm.hist[bin_slot<kB>((key[i] >> shift) & static_cast<uint32_t>(nb - 1))], 1u);
             }
-            thr = sm.prefix;
-            need = sm.need;
+            __syncthreads();
+            // thread t: bins nb-1-t*B-b, b = 0 .. B-1, counted from the top
+            uint32_t cnt[kB], sum = 0u;
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int d = nb - 1 - tid * kB - b;
+                cnt[b] = d >= 0 ? sm.hist[bin_slot<kB>(static_cast<uint32_t>(d))] : 0u;
+                sum += cnt[b];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (lane == 31) sm.warp_sum[warp] = incl;
+            const uint32_t want = sm.need;
+            __syncthreads();
+#pragma unroll
+            for (int b = 0; b < kB; ++b) sm.hist[bin_slot<kB>(tid * kB + b)] = 0u;
+            uint32_t before = 0u;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) before += w < warp ? sm.warp_sum[w] : 0u;
+            const uint32_t excl = before + incl - sum;
+            if (excl < want && want <= excl + sum) {
+                uint32_t above = excl;
+#pragma unroll
+                for (int b = 0; b < kB; ++b) {
+                    if (above + cnt[b] >= want) {
+                        const uint32_t d = static_cast<uint32_t>(nb - 1 - tid * kB - b);
+                        sm.prefix = prefix | (d << shift);
+                        sm.need = want - above;
+                        sm.done = above + cnt[b] == want ? 1u : 0u;
+                        break;
+                    }
+                    above += cnt[b];
+                }
+            }
+            __syncthreads();
+            if (sm.done) break;
+        }
+        // picks: the keys > thr, and the first `need` keys == thr
+        uint32_t thr = sm.prefix, need = sm.need;
+        if (sm.done) {
+            // every key of the chosen bin is a pick: the picks are the keys >=
+            // prefix (never 0 here: that bin would hold every candidate)
+            need = thr == 0u ? 0xFFFFFFFFu : 0u;
+            thr = thr == 0u ? 0u : thr - 1u;
         }
 
-        // 3. count the picks of this warp's share, prefix over the warps,
-        //    then write them in position order
-        uint32_t c_gt = 0u, c_eq = 0u;
+        // 3. this thread's keys above thr and equal to thr, packed; block scan
+        uint32_t packed = 0u;
+        if (need == 0u) {
 #pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int j = j_lo + lane + 32 * i;
-            c_gt += __popc(__ballot_sync(0xFFFFFFFFu, j < j_hi && (all || key[i] > thr)));
-            c_eq += __popc(__ballot_sync(0xFFFFFFFFu, j < j_hi && !all && key[i] == thr));
+            for (int i = 0; i < kTopkPerThread; ++i) packed += key[i] > thr ? 0x10000u : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kTopkPerThread; ++i) packed += key[i] > thr ? 0x10000u : (key[i] == thr ? 1u : 0u);
         }
-        if (lane == 0) {
-            sm.warp_sum[warp] = c_gt;
-            sm.warp_eq[warp] = c_eq;
+        uint32_t incl = packed;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
         }
+        if (lane == 31) sm.warp_sum[warp] = incl;
         __syncthreads();
-        uint32_t eq_before = 0u, out_at = 0u;     // over the shares before this one
-        for (int w = 0; w < warp; ++w) {
-            const uint32_t eq_w = sm.warp_eq[w];
-            const uint32_t taken = eq_before >= need ? 0u : min(eq_w, need - eq_before);
-            out_at += sm.warp_sum[w] + taken;
-            eq_before += eq_w;
-        }
+        uint32_t before = incl - packed;
 #pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int j = j_lo + lane + 32 * i;
-            const bool gt = j < j_hi && (all || key[i] > thr);
-            const bool eq = j < j_hi && !all && key[i] == thr;
-            const uint32_t be = __ballot_sync(0xFFFFFFFFu, eq);
-            const bool pick = gt || (eq && eq_before + __popc(be & lt_mask) < need);
-            const uint32_t bp = __ballot_sync(0xFFFFFFFFu, pick);
-            if (pick) out[out_at + __popc(bp & lt_mask)] = j;
-            out_at += __popc(bp);
-            eq_before += __popc(be);
+        for (int w = 0; w < kWarps; ++w) before += w < warp ? sm.warp_sum[w] : 0u;
+        const uint32_t eq_before = before & 0xFFFFu;
+        int at = static_cast<int>((before >> 16) + (eq_before < need ? eq_before : need));
+        // writes pick i at output entry `at`
+        auto put = [&](int i, int a) {
+            if (kMode == kRowsToIdx) {
+                out[a] = j0 + i;
+            } else if (kMode == kSharesToCand) {
+                cand_key[at0 + a] = key[i];
+                cand_pos[at0 + a] = share0 + j0 + i;
+            } else {
+                out[a] = cand_pos[j0 + i];
+            }
+        };
+        if (need == 0u) {
+#pragma unroll
+            for (int i = 0; i < kTopkPerThread; ++i) {
+                if (key[i] > thr) put(i, at++);
+            }
+        } else {
+            uint32_t eq_seen = eq_before;
+#pragma unroll
+            for (int i = 0; i < kTopkPerThread; ++i) {
+                const bool eq = key[i] == thr;
+                if (key[i] > thr || (eq && eq_seen < need)) put(i, at++);
+                eq_seen += eq ? 1u : 0u;
+            }
         }
-        for (int j = m + tid; j < p.k_max; j += kThreads) out[j] = -1;
-        if (tid == 0) p.n_sel[r] = m;
-        __syncthreads();             // the shared state is rewritten by the next row
+        if (kMode != kSharesToCand) {
+            for (int j = m + tid; j < p.k_max; j += kThreads) out[j] = -1;
+            if (tid == 0) p.n_sel[r] = m;
+        }
+        __syncthreads();             // warp_sum and the select state are rewritten by the next segment
     }
 }
 
-}  // namespace
-
-cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t s) {
+template <int kThreads, int kMode>
+cudaError_t launch_mode(const TopkParams& p, int grid, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.ld <= 256 * 16) {
-        cfg.blockDim = dim3(256);
-        return cudaLaunchKernelEx(&cfg, dsa_topk_kernel<256, 16>, p);
-    }
-    if (p.ld > kTopkMaxLd) return cudaErrorInvalidValue;
-    cfg.blockDim = dim3(1024);
-    return cudaLaunchKernelEx(&cfg, dsa_topk_kernel<1024, 32>, p);
+    return cudaLaunchKernelEx(&cfg, dsa_topk_kernel<kThreads, kMode>, p);
+}
+
+}  // namespace
+
+int topk_shares(int ld) { return ld <= kTopkShare ? 1 : (ld + kTopkShare - 1) / kTopkShare; }
+
+cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t s) {
+    if (p.ld % 4 != 0 || reinterpret_cast<uintptr_t>(p.scores) % 16 != 0 || p.ld > kTopkMaxLd)
+        return cudaErrorInvalidValue;
+    if (p.shares == 1) return launch_mode<256, kRowsToIdx>(p, grid, s);
+    // long rows: the shares' selections, then one over their picks
+    if (p.cand_ld % 4 != 0 || p.cand_ld < p.shares * p.k || p.shares * p.k > 1024 * kTopkPerThread)
+        return cudaErrorInvalidValue;
+    const long long share_grid = static_cast<long long>(grid) * p.shares;
+    cudaError_t e = launch_mode<256, kSharesToCand>(p, static_cast<int>(share_grid), s);
+    if (e != cudaSuccess) return e;
+    const int cap = p.shares * p.k;
+    if (cap <= 256 * kTopkPerThread) return launch_mode<256, kCandToIdx>(p, grid, s);
+    if (cap <= 512 * kTopkPerThread) return launch_mode<512, kCandToIdx>(p, grid, s);
+    return launch_mode<1024, kCandToIdx>(p, grid, s);
 }
 
 }  // namespace dsa

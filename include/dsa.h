@@ -36,7 +36,8 @@
  *   nothing per call: a small device block (the error word and up to 64
  *   two-int row queues) and, for decode, one scratch buffer for split partial
  *   results are allocated once per device on first use (the scratch grows
- *   when a larger batch needs it) and released by dsa_shutdown().  Do not
+ *   when a larger batch needs it; dsa_topk_select has one of its own) and
+ *   released by dsa_shutdown().  Do not
  *   issue the first call of a device inside a CUDA graph capture.  Decode
  *   calls whose work overlaps on the GPU (other streams, other threads) share
  *   that scratch and race; order them on one stream.
@@ -207,6 +208,11 @@ DSA_API dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_
  * no input before the work queued before it on the stream has completed.
  * DSA_ERR_INVALID_ARG for a null pointer, a misaligned scores, or bad
  * sizes; DSA_ERR_UNSUPPORTED for k > 2048 or ld > 32768.
+ * Rows with ld > 4096 are selected in two steps (each 4096-position share
+ * of a row, then the shares' picks) through a per-device scratch of up to
+ * 256 MB, allocated on first use (a larger call processes its rows in turn)
+ * and released by dsa_shutdown(); such calls whose work overlaps on the GPU
+ * share that scratch and race: order them on one stream.
  */
 DSA_API dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, int R,
                                    int k, int32_t* idx, int k_max, int32_t* n_sel,

@@ -75,6 +75,17 @@ def test_ties_signed_zeros_infinities_and_nans(k):
     assert code == 0
 
 
+@pytest.mark.parametrize("k", [7, 640, 2048])
+def test_specials_on_rows_split_over_a_cluster(k):
+    # ties, signed zeros, infinities and NaNs whose runs cross the CTAs of a row
+    rng = np.random.default_rng(5050 + k)
+    R, ld = 6, 9000
+    scores = special_scores(rng, (R, ld))
+    n_valid = np.array([k - 1, k + 1, 4096, 4097, 8999, 9000], np.int32)
+    code, _ = check(scores, n_valid, k, k + 5)
+    assert code == 0
+
+
 def test_all_scores_equal_and_all_nan():
     scores = np.zeros((3, 1024), np.float32)
     scores[1] = np.nan
@@ -88,6 +99,19 @@ def test_long_rows_and_row_stride():
     scores = rng.standard_normal((4, 32768), dtype=np.float32)
     scores[:, 1000:1100] = 7.0        # ties at the top
     code, _ = check(scores, np.array([32768, 30000, 641, 640], np.int32), 640, 700)
+    assert code == 0
+
+
+@pytest.mark.parametrize("ld", [3000, 4092, 4096, 4100, 5000, 12000, 28676])
+def test_row_strides_and_ragged_tails(ld):
+    # row strides on both sides of 4096 (one CTA a row below, a cluster of
+    # ceil(ld / 4096) CTAs a row above), candidate
+    # counts ending at every offset within a float4 and within a thread's run
+    rng = np.random.default_rng(5150 + ld)
+    scores = rng.standard_normal((8, ld), dtype=np.float32)
+    scores[:, 5:40] = 1.5             # ties straddling the threshold
+    n_valid = np.array([ld, ld - 1, ld - 2, ld - 3, ld - 17, 641, 700, 3], np.int32)
+    code, _ = check(scores, n_valid, 640)
     assert code == 0
 
 
