@@ -35,6 +35,8 @@ from deepseek_v4_top_gb300 import inputs as I  # noqa: E402
 
 H, D, K = 64, 512, 640
 E2E_CHUNKS = 8                              # prefill row chunks in the end-to-end step
+OPROJ_D_OUT = 7168                          # output projection width timed (DeepSeek-V3's model width;
+                                            # the pages give none for V4.1)
 DEC_B, DEC_N = 8, 32768
 PRE_R, PRE_N = 2048, 4096
 METRIC = "sparse-attn row·heads/s and HBM GB/s at H=64,d=512,k=640 (decode B=8, prefill 2048)"
@@ -261,6 +263,47 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
     ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     assert dsa.dsa_get_device_error() == 0
     return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
+
+
+def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
+    """The prefill rows' attention with a bf16 output, then their output
+    projection (out [2048, d_out] fp32 = attn [2048, 64*512] bf16 . w_o), each
+    call alone with the L2 flushed before it.  w_o is seeded N(0, 1/K) on the
+    device (the pages give no projection weights or width).  Returns (attention
+    ms, projection ms)."""
+    import torch
+    K = H * D
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xD5A0 + 17)
+    w_o = (torch.randn((K, d_out), generator=g, device=dev) * K ** -0.5).to(torch.bfloat16)
+    attn = torch.empty((PRE_R, H, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((PRE_R, d_out), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call_attn():
+        dsa.dsa_sparse_attn(d_pre["q"], d_pre["kv"], d_pre["idx"], d_pre["n_sel"], d_pre["sink"], pre.scale,
+                            attn, 0, stream)
+
+    def call_proj():
+        dsa.dsa_oproj(attn, w_o, out, stream)
+
+    res = []
+    for fn in (call_attn, call_proj):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        hold_gpu(stream)
+        for i in range(reps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        res.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps)
+    assert dsa.dsa_get_device_error() == 0
+    assert torch.isfinite(out).all().item()
+    return res[0], res[1]
 
 
 def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
@@ -504,6 +547,22 @@ def bench_ours(args, world, rank, local):
                 "scores_gbs": nbytes / (t_ms * 1e-3) / 1e9,
                 "scores_frac_hbm": nbytes / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                 "how": "dsa_topk_select, k=%d, N(0,1) scores, one call a time, L2 flushed before each" % K}
+    if do_pre:
+        # the prefill rows with a bf16 output, then their output projection
+        a_ms, p_ms = oproj_timing(dsa, dev, flush, d_pre, pre)
+        a_ms, p_ms = reduce_max(a_ms, world), reduce_max(p_ms, world)
+        g = PRE_R * K * D * 2
+        workloads["prefill_2048_bf16_out"] = {
+            "ms": a_ms, "row_heads_per_s": PRE_R * H / (a_ms * 1e-3),
+            "gathered_frac_hbm": g / (a_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "how": "dsa_sparse_attn, out bf16 [2048, 64, 512] (134 MB instead of 268 MB fp32), one call a time, "
+                   "L2 flushed before each"}
+        p_flops = 2.0 * PRE_R * H * D * OPROJ_D_OUT
+        workloads["oproj_2048x32768x%d" % OPROJ_D_OUT] = {
+            "ms": p_ms, "tflops": p_flops / (p_ms * 1e-3) / 1e12,
+            "frac_bf16_peak": p_flops / (p_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "how": "dsa_oproj (cuBLASLt, bf16 x bf16 -> fp32): the 2048 rows' bf16 attention output times a "
+                   "seeded [32768, %d] bf16 projection, one call a time, L2 flushed before each" % OPROJ_D_OUT}
     roofline = None
     if do_pre:
         g = PRE_R * K * D * 2

@@ -1,8 +1,8 @@
 """Builds libdsa.so in-tree with nvcc for sm_103a (no torch extension machinery).
 
-The three CUDA translation units compile in parallel; the shared library
-links the CUDA runtime statically and exports only the C ABI of
-include/dsa.h.
+The CUDA translation units compile in parallel; the shared library links
+the CUDA runtime statically and cuBLASLt (the output projection's GEMM)
+dynamically, and exports only the C ABI of include/dsa.h.
 """
 
 from __future__ import annotations
@@ -65,7 +65,7 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-lcublasLt", "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

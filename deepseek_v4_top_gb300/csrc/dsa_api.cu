@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include <cublasLt.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dsa.h"
@@ -24,6 +25,8 @@ struct DeviceState {
     size_t scratch_bytes = 0;
     void* topk_scratch = nullptr;  // two-step top-k: the shares' picks
     size_t topk_scratch_bytes = 0;
+    cublasLtHandle_t lt = nullptr;  // the output projection's GEMM
+    void* lt_work = nullptr;
     int sm_count = 0;
     cudaStream_t queue_stream[kQueues] = {};
     int queues_used = 0;
@@ -89,6 +92,77 @@ dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
     return r;
 }
 
+// The output projection: out [R][d_out] fp32 = attn [R][K] bf16 . w_o [K][d_out]
+// bf16, accumulated in fp32 by cuBLASLt (a plain library GEMM).  Row-major
+// C = A.B is column-major C^T = B^T.A^T, so cuBLASLt sees m = d_out, n = R,
+// k = K with its A = w_o (ld d_out), its B = attn (ld K) and C = out (ld
+// d_out).  Only algorithms without a split-K reduction are taken, so a
+// call's result does not depend on the run.  The handle and a 32 MB
+// workspace are made once per device.
+constexpr size_t kLtWorkBytes = static_cast<size_t>(32) << 20;
+
+dsa_status oproj_gemm(DeviceState* ds, const void* attn, const void* w_o, float* out, int R, int K, int d_out,
+                      cudaStream_t s) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!ds->lt) {
+            if (cublasLtCreate(&ds->lt) != CUBLAS_STATUS_SUCCESS) {
+                ds->lt = nullptr;
+                return DSA_ERR_CUDA;
+            }
+            if (cudaMalloc(&ds->lt_work, kLtWorkBytes) != cudaSuccess) {
+                cublasLtDestroy(ds->lt);
+                ds->lt = nullptr;
+                ds->lt_work = nullptr;
+                return DSA_ERR_CUDA;
+            }
+        }
+    }
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    dsa_status st = DSA_ERR_CUDA;
+    do {
+        if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) break;
+        const cublasOperation_t no_t = CUBLAS_OP_N;
+        if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &no_t, sizeof(no_t)) !=
+                CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &no_t, sizeof(no_t)) !=
+                CUBLAS_STATUS_SUCCESS)
+            break;
+        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, d_out, K, d_out) != CUBLAS_STATUS_SUCCESS) break;
+        if (cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, K, R, K) != CUBLAS_STATUS_SUCCESS) break;
+        if (cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, d_out, R, d_out) != CUBLAS_STATUS_SUCCESS) break;
+        if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
+        const size_t ws = kLtWorkBytes;
+        const uint32_t no_split = CUBLASLT_REDUCTION_SCHEME_NONE;
+        if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws,
+                                                 sizeof(ws)) != CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &no_split,
+                                                 sizeof(no_split)) != CUBLAS_STATUS_SUCCESS)
+            break;
+        cublasLtMatmulHeuristicResult_t h = {};
+        int found = 0;
+        if (cublasLtMatmulAlgoGetHeuristic(ds->lt, op, la, lb, lc, lc, pref, 1, &h, &found) !=
+                CUBLAS_STATUS_SUCCESS ||
+            found == 0) {
+            st = DSA_ERR_UNSUPPORTED;
+            break;
+        }
+        const float one = 1.0f, zero = 0.0f;
+        if (cublasLtMatmul(ds->lt, op, &one, w_o, la, attn, lb, &zero, out, lc, out, lc, &h.algo, ds->lt_work,
+                           kLtWorkBytes, s) != CUBLAS_STATUS_SUCCESS)
+            break;
+        st = DSA_OK;
+    } while (false);
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (lc) cublasLtMatrixLayoutDestroy(lc);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    return st;
+}
+
 // The row queue of stream s, or null (round-robin rows) when s may run on
 // several threads' behalf at once (the per-thread default stream), while s
 // is being captured into a graph (a replay could overlap other work that
@@ -113,7 +187,7 @@ int* stream_queue(DeviceState* st, cudaStream_t s) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
-                      const float* sink, const float* out, int R, int H, int N, int k_max,
+                      const float* sink, const void* out, int R, int H, int N, int k_max,
                       dsa_dtype dtype, int decode) {
     if (R < 0 || N <= 0 || k_max <= 0 || H <= 0) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
@@ -134,10 +208,12 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
 // decode: 0 for prefill (one cache shared by every row), T >= 1 for decode
 // with T query rows a slot (row r reads slot r / T).
 dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
-               const float* sink, float scale, float* out, int R, int H, int N, int k_max,
-               dsa_dtype dtype, void* stream, int decode) {
+               const float* sink, float scale, void* out, int R, int H, int N, int k_max,
+               dsa_dtype dtype, void* stream, int decode, dsa_dtype out_dtype = DSA_F32) {
+    if (out_dtype != DSA_F32 && out_dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
     dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype, decode);
     if (st != DSA_OK || R == 0) return st;
+    const int out_bf16 = out_dtype == DSA_BF16 ? 1 : 0;
     DeviceState* ds = nullptr;
     st = device_state(&ds);
     if (st != DSA_OK) return st;
@@ -151,6 +227,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
         p.n_sel = n_sel;
         p.sink = sink;
         p.out = out;
+        p.out_bf16 = out_bf16;
         p.err = ds->err;
         p.scale = scale;
         p.R = R;
@@ -168,6 +245,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     p.n_sel = n_sel;
     p.sink = sink;
     p.out = out;
+    p.out_bf16 = out_bf16;
     p.part = nullptr;
     p.err = ds->err;
     p.queue = nullptr;
@@ -198,6 +276,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
         c.part = p.part;
         c.sink = sink;
         c.out = out;
+        c.out_bf16 = out_bf16;
         c.R = R;
         c.H = H;
         c.chunks = chunks;
@@ -230,6 +309,40 @@ dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache, const in
                                    const int32_t* n_sel, const float* sink, float scale, float* out,
                                    int R, int H, int N, int k_max, dsa_dtype dtype, void* stream) {
     return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, 0);
+}
+
+dsa_status dsa_sparse_attn(const void* q, const void* kv_cache, const int32_t* idx, const int32_t* n_sel,
+                           const float* sink, float scale, void* out, int R, int rows_per_slot, int H,
+                           int N, int k_max, dsa_dtype dtype, dsa_dtype out_dtype, void* stream) {
+    if (R < 0 || rows_per_slot < 0 || (rows_per_slot > 0 && R % rows_per_slot != 0)) return DSA_ERR_INVALID_ARG;
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, rows_per_slot,
+                    out_dtype);
+}
+
+dsa_status dsa_oproj(const void* attn, const void* w_o, float* out, int R, int K, int d_out, void* stream) {
+    if (R < 0 || K <= 0 || d_out <= 0) return DSA_ERR_INVALID_ARG;
+    if (R == 0) return DSA_OK;
+    if (!attn || !w_o || !out) return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(attn) || !dsa::aligned16(w_o) || !dsa::aligned16(out) || K % 8 != 0 || d_out % 8 != 0)
+        return DSA_ERR_INVALID_ARG;
+    dsa::DeviceState* ds = nullptr;
+    dsa_status st = dsa::device_state(&ds);
+    if (st != DSA_OK) return st;
+    return dsa::oproj_gemm(ds, attn, w_o, out, R, K, d_out, static_cast<cudaStream_t>(stream));
+}
+
+dsa_status dsa_sparse_attn_prefill_oproj(const void* q, const void* kv_cache, const int32_t* idx,
+                                         const int32_t* n_sel, const float* sink, float scale,
+                                         const void* w_o, void* attn, float* out, int R, int H, int N,
+                                         int k_max, int d_out, void* stream) {
+    if (R < 0 || H <= 0 || d_out <= 0) return DSA_ERR_INVALID_ARG;
+    if (R == 0) return DSA_OK;
+    if (!w_o || !attn || !out) return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(w_o) || !dsa::aligned16(out) || d_out % 8 != 0) return DSA_ERR_INVALID_ARG;
+    dsa_status st = dsa::run(q, kv_cache, idx, n_sel, sink, scale, attn, R, H, N, k_max, DSA_BF16, stream, 0,
+                             DSA_BF16);
+    if (st != DSA_OK) return st;
+    return dsa_oproj(attn, w_o, out, R, H * dsa::kD, d_out, stream);
 }
 
 dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n_valid, int R, int k,
@@ -324,7 +437,7 @@ dsa_status dsa_shutdown(void) {
     dsa_status st = DSA_OK;
     for (int d = 0; d < dsa::kMaxDevices; ++d) {
         dsa::DeviceState& ds = dsa::g_dev[d];
-        if (!ds.err && !ds.scratch && !ds.topk_scratch) continue;
+        if (!ds.err && !ds.scratch && !ds.topk_scratch && !ds.lt) continue;
         if (cudaSetDevice(d) != cudaSuccess) {
             st = DSA_ERR_CUDA;
             continue;
@@ -332,6 +445,8 @@ dsa_status dsa_shutdown(void) {
         if (ds.err) cudaFree(ds.err);
         if (ds.scratch) cudaFree(ds.scratch);
         if (ds.topk_scratch) cudaFree(ds.topk_scratch);
+        if (ds.lt_work) cudaFree(ds.lt_work);
+        if (ds.lt) cublasLtDestroy(ds.lt);
         ds = dsa::DeviceState();
     }
     if (have_cur) cudaSetDevice(cur);

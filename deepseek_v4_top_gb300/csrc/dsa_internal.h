@@ -28,7 +28,8 @@ struct TcParams {
     const int32_t* idx;       // [R][k_max]
     const int32_t* n_sel;     // [R]
     const float* sink;        // [H]
-    float* out;               // final mode: [R][H][512]
+    void* out;                // final mode: [R][H][512], fp32 or (out_bf16) bf16
+    int out_bf16;
     float* part;              // partial mode: O [units][64][512] then (m, l) [units][2][64]
     uint32_t* err;            // device error word
     int* queue;               // null: units round-robin over the grid; else the launch's unit
@@ -48,7 +49,8 @@ struct SimtParams {
     const int32_t* idx;
     const int32_t* n_sel;
     const float* sink;
-    float* out;
+    void* out;                // [R][H][512], fp32 or (out_bf16) bf16
+    int out_bf16;
     uint32_t* err;
     float scale;
     int R, H, N, k_max;
@@ -58,7 +60,8 @@ struct SimtParams {
 struct CombineParams {
     const float* part;        // as TcParams::part
     const float* sink;
-    float* out;
+    void* out;                // [R][H][512], fp32 or (out_bf16) bf16
+    int out_bf16;
     int R, H, chunks, units;
 };
 

@@ -104,6 +104,7 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
     p.n_sel = n_sel;
     p.sink = sink;
     p.out = out;
+    p.out_bf16 = 0;
     p.part = d->base + kHeaderFloats;
     p.err = err;
     p.queue = nullptr;
@@ -124,6 +125,7 @@ extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* 
         c.part = p.part;
         c.sink = sink;
         c.out = out;
+        c.out_bf16 = 0;
         c.R = B;
         c.H = H;
         c.chunks = p.chunks;

@@ -10,6 +10,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cuda_bf16.h>
+
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
 
@@ -107,9 +109,16 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
     const float e1 = expf(mu - mstar);
     const float e2 = expf(sk - mstar);
     const float f = e1 / (l * e1 + e2);
-    float* orow = p.out + (static_cast<size_t>(r) * p.H + h) * kD;
+    const size_t o0 = (static_cast<size_t>(r) * p.H + h) * kD;
+    if (p.out_bf16) {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + o0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = acc[i] * f;
+        for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = __float2bfloat16_rn(acc[i] * f);
+    } else {
+        float* orow = static_cast<float*>(p.out) + o0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = acc[i] * f;
+    }
 }
 
 // One CTA per (row, head); thread t owns columns 4t .. 4t+3.  Partials of
@@ -173,8 +182,15 @@ __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p)
     const float e1 = exp2f(mu - mstar);
     const float e2 = exp2f(s2 - mstar);
     const float f = e1 / (l * e1 + e2);
-    float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
-    reinterpret_cast<float4*>(p.out + (static_cast<size_t>(r) * p.H + h) * kD)[tid] = res;
+    const float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+    const size_t o0 = (static_cast<size_t>(r) * p.H + h) * kD;
+    if (p.out_bf16) {
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o0) + 2 * tid;
+        o2[0] = __floats2bfloat162_rn(res.x, res.y);
+        o2[1] = __floats2bfloat162_rn(res.z, res.w);
+    } else {
+        reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0)[tid] = res;
+    }
 }
 
 }  // namespace

@@ -833,8 +833,12 @@ __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, 
         if (lane == 0) mbar_arrive(smem_addr(&ms.l_free));
         if (!mbar_wait(smem_addr(&ms.o_full), nu & 1, ab, p.err)) return;
         tc_fence_after();
-        float* dst = p.partial ? p.part + static_cast<size_t>(u) * kHeadsPad * kD
-                               : p.out + static_cast<size_t>(u / p.chunks) * p.H * kD;
+        // fp32 (partials, or the final output) or bf16 (final output, rounded to nearest even)
+        const size_t dst_off = p.partial ? static_cast<size_t>(u) * kHeadsPad * kD
+                                         : static_cast<size_t>(u / p.chunks) * p.H * kD;
+        float* dst = (p.partial ? p.part : static_cast<float*>(p.out)) + dst_off;
+        __nv_bfloat16* dst16 = static_cast<__nv_bfloat16*>(p.out) + dst_off;
+        const bool to_bf16 = !p.partial && p.out_bf16;
         const int d0 = 32 * qd + lane;
 #pragma unroll 1
         for (int hg = 0; hg < 4; ++hg) {
@@ -854,10 +858,18 @@ __device__ void output_role(const TcParams& p, Misc& ms, uint32_t tmem, int qd, 
                     for (int j = 0; j < 16; ++j) o[j] += lo[j];
                 }
                 const int d = i * 128 + d0;
+                if (to_bf16) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int h = 16 * hg + j;
-                    if (h < p.H) dst[static_cast<size_t>(h) * kD + d] = o[j] * fh[j];
+                    for (int j = 0; j < 16; ++j) {
+                        const int h = 16 * hg + j;
+                        if (h < p.H) dst16[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(o[j] * fh[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int h = 16 * hg + j;
+                        if (h < p.H) dst[static_cast<size_t>(h) * kD + d] = o[j] * fh[j];
+                    }
                 }
             }
         }

@@ -32,6 +32,7 @@ DSA_DEVERR_NVALID_RANGE = 0x10
 
 # Every function declared in include/dsa.h.
 EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_decode_rows", "dsa_sparse_attn_prefill",
+           "dsa_sparse_attn", "dsa_oproj", "dsa_sparse_attn_prefill_oproj",
            "dsa_sparse_attn_decode_noalloc",
            "dsa_topk_select", "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string",
            "dsa_shutdown")
@@ -64,6 +65,12 @@ def load():
                 fn.restype = I
             lib.dsa_sparse_attn_decode_rows.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, P]
             lib.dsa_sparse_attn_decode_rows.restype = I
+            lib.dsa_sparse_attn.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, P]
+            lib.dsa_sparse_attn.restype = I
+            lib.dsa_oproj.argtypes = [P, P, P, I, I, I, P]
+            lib.dsa_oproj.restype = I
+            lib.dsa_sparse_attn_prefill_oproj.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I, I, P]
+            lib.dsa_sparse_attn_prefill_oproj.restype = I
             lib.dsa_topk_select.argtypes = [P, I, P, I, I, P, I, P, P]
             lib.dsa_topk_select.restype = I
             lib.dsa_selftest_wait_limit.argtypes = [P]
@@ -101,7 +108,7 @@ def _dtype_code(t):
     raise TypeError("q and kv_cache must be float32 or bfloat16, got %s" % t.dtype)
 
 
-def _check(q, kv, idx, n_sel, sink, out, decode, rows_per_slot=1):
+def _check(q, kv, idx, n_sel, sink, out, decode, rows_per_slot=1, out_dtype=None):
     import torch
     for name, t in (("q", q), ("kv_cache", kv), ("idx", idx), ("n_sel", n_sel), ("sink", sink),
                     ("out", out)):
@@ -115,8 +122,10 @@ def _check(q, kv, idx, n_sel, sink, out, decode, rows_per_slot=1):
         raise TypeError("q and kv_cache must have the same dtype")
     if idx.dtype != torch.int32 or n_sel.dtype != torch.int32:
         raise TypeError("idx and n_sel must be int32")
-    if sink.dtype != torch.float32 or out.dtype != torch.float32:
-        raise TypeError("sink and out must be float32")
+    if sink.dtype != torch.float32:
+        raise TypeError("sink must be float32")
+    if out.dtype != (torch.float32 if out_dtype is None else out_dtype):
+        raise TypeError("out must be %s" % ("float32" if out_dtype is None else out_dtype))
     if q.dim() != 3 or q.shape[2] != 512:
         raise ValueError("q must be [rows, heads, 512]")
     R, H = q.shape[0], q.shape[1]
@@ -178,6 +187,67 @@ def dsa_sparse_attn_decode_rows(q, kv_cache, idx, n_sel, sink, scale, out, rows_
 def dsa_sparse_attn_prefill(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):
     """Prefill attention: q [R,H,512], kv_cache [N,512], out [R,H,512] fp32."""
     return _run("dsa_sparse_attn_prefill", False, q, kv_cache, idx, n_sel, sink, scale, out, stream)
+
+
+def dsa_sparse_attn(q, kv_cache, idx, n_sel, sink, scale, out, rows_per_slot=0, stream=None):
+    """Attention with the output type taken from `out` (float32 or bfloat16):
+    rows_per_slot 0 is prefill (kv_cache [N,512]), T >= 1 decode with T rows a
+    slot (kv_cache [R/T,N,512]).  A bf16 out holds the float32 result rounded
+    to nearest even."""
+    import torch
+    T = int(rows_per_slot)
+    if T < 0:
+        raise ValueError("rows_per_slot must be >= 0")
+    if not isinstance(out, torch.Tensor) or out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be a float32 or bfloat16 tensor")
+    R, H, N, k_max = _check(q, kv_cache, idx, n_sel, sink, out, decode=T > 0, rows_per_slot=max(T, 1),
+                            out_dtype=out.dtype)
+    st = load().dsa_sparse_attn(q.data_ptr(), kv_cache.data_ptr(), idx.data_ptr(), n_sel.data_ptr(),
+                                sink.data_ptr(), ctypes.c_float(float(scale)), out.data_ptr(), R, T, H, N,
+                                k_max, _dtype_code(q), _dtype_code(out), _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_sparse_attn")
+    return out
+
+
+def _check_oproj(attn, w_o, out):
+    import torch
+    for name, t in (("attn", attn), ("w_o", w_o), ("out", out)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if attn.dtype != torch.bfloat16 or w_o.dtype != torch.bfloat16 or out.dtype != torch.float32:
+        raise TypeError("attn and w_o must be bfloat16, out float32")
+    if w_o.dim() != 2 or out.dim() != 2:
+        raise ValueError("w_o [K, d_out] and out [rows, d_out] expected")
+    R, K, d_out = attn.shape[0], w_o.shape[0], w_o.shape[1]
+    if attn.numel() != R * K or tuple(out.shape) != (R, d_out):
+        raise ValueError("attn [rows, K] (or [rows, H, 512] with H*512 = K) and out [rows, d_out] expected")
+    return R, K, d_out
+
+
+def dsa_oproj(attn, w_o, out, stream=None):
+    """Output projection: out [R,d_out] fp32 = attn [R,K] bf16 . w_o [K,d_out] bf16."""
+    R, K, d_out = _check_oproj(attn, w_o, out)
+    st = load().dsa_oproj(attn.data_ptr(), w_o.data_ptr(), out.data_ptr(), R, K, d_out, _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_oproj")
+    return out
+
+
+def dsa_sparse_attn_prefill_oproj(q, kv_cache, idx, n_sel, sink, scale, w_o, attn, out, stream=None):
+    """Prefill attention (bf16 q/kv) into attn [R,H,512] bf16, then
+    out [R,d_out] fp32 = attn . w_o [H*512,d_out] bf16."""
+    R, H, N, k_max = _check(q, kv_cache, idx, n_sel, sink, attn, decode=False, out_dtype=attn.dtype)
+    R2, K, d_out = _check_oproj(attn, w_o, out)
+    if K != H * 512 or R2 != R:
+        raise ValueError("w_o must be [heads * 512, d_out]")
+    st = load().dsa_sparse_attn_prefill_oproj(q.data_ptr(), kv_cache.data_ptr(), idx.data_ptr(), n_sel.data_ptr(),
+                                              sink.data_ptr(), ctypes.c_float(float(scale)), w_o.data_ptr(),
+                                              attn.data_ptr(), out.data_ptr(), R, H, N, k_max, d_out,
+                                              _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_sparse_attn_prefill_oproj")
+    return out
 
 
 def dsa_sparse_attn_decode_noalloc(q, kv_cache, idx, n_sel, sink, scale, out, stream=None):

@@ -149,6 +149,57 @@ DSA_API dsa_status dsa_sparse_attn_prefill(const void* q, const void* kv_cache,
                                            dsa_dtype dtype, void* stream);
 
 /*
+ * The three calls above in one, with the output type chosen:
+ *   rows_per_slot 0   prefill: every row reads the one cache kv [N][512];
+ *   rows_per_slot T   decode: row r reads slot r / T of kv [R/T][N][512]
+ *                     (R a multiple of T).
+ *   out_dtype DSA_F32   out [R][H][512] float32, as the calls above;
+ *   out_dtype DSA_BF16  out [R][H][512] bfloat16: each element is the float32
+ *                       result of the same call rounded to nearest even,
+ *                       bit for bit.  Half the bytes, and the A operand of
+ *                       dsa_oproj as it stands.
+ * Otherwise as dsa_sparse_attn_prefill / _decode_rows (out 16-byte aligned).
+ */
+DSA_API dsa_status dsa_sparse_attn(const void* q, const void* kv_cache,
+                                   const int32_t* idx, const int32_t* n_sel,
+                                   const float* sink, float scale, void* out,
+                                   int R, int rows_per_slot, int H, int N, int k_max,
+                                   dsa_dtype dtype, dsa_dtype out_dtype, void* stream);
+
+/*
+ * Output projection of attention rows (the step after the attention: the
+ * heads' outputs of a row, concatenated, times the projection matrix):
+ *   attn [R][K] bfloat16 (for this library's output, K = H*512 and the
+ *        [R][H][512] bf16 out of dsa_sparse_attn),
+ *   w_o  [K][d_out] bfloat16, row-major,
+ *   out  [R][d_out] float32 = attn . w_o, accumulated in float32.
+ * A plain GEMM, run by cuBLASLt (no split-K reduction, so repeated calls
+ * give the same bits).  The pages give no shape for this projection;
+ * d_out is the caller's.  All three 16-byte aligned, K and d_out multiples
+ * of 8.  The first call on a device creates a cuBLASLt handle and a 32 MB
+ * workspace, kept until dsa_shutdown(); calls whose work overlaps on the GPU
+ * share that workspace and race: order them on one stream.
+ * DSA_ERR_INVALID_ARG for null pointers or bad sizes, DSA_ERR_UNSUPPORTED if
+ * cuBLASLt offers no algorithm, DSA_ERR_CUDA if it fails.
+ */
+DSA_API dsa_status dsa_oproj(const void* attn, const void* w_o, float* out,
+                             int R, int K, int d_out, void* stream);
+
+/*
+ * Prefill attention with its output projection: dsa_sparse_attn with bf16
+ * inputs, rows_per_slot 0 and out_dtype DSA_BF16 into the caller's buffer
+ * attn [R][H][512] bfloat16, then dsa_oproj(attn, w_o, out, R, H*512, d_out)
+ * on the same stream.  The attention's rows go to the GEMM as bf16, half the
+ * bytes of the float32 output.
+ */
+DSA_API dsa_status dsa_sparse_attn_prefill_oproj(const void* q, const void* kv_cache,
+                                                 const int32_t* idx, const int32_t* n_sel,
+                                                 const float* sink, float scale,
+                                                 const void* w_o, void* attn, float* out,
+                                                 int R, int H, int N, int k_max, int d_out,
+                                                 void* stream);
+
+/*
  * Largest number of (row, 128-key chunk) units that
  * dsa_sparse_attn_decode_noalloc() accepts: B * ceil(k_max / 128) <= 64,
  * e.g. 8 rows with k_max <= 1024.

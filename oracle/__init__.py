@@ -6,4 +6,4 @@ no code with the CUDA path.  See ``dsa_oracle.h`` for the definition and the
 passages it follows.
 """
 
-from .oracle import build, load, attn, pairs, rowhead, max_threads, topk, LIB_PATH  # noqa: F401
+from .oracle import build, load, attn, pairs, rowhead, max_threads, topk, oproj, LIB_PATH  # noqa: F401

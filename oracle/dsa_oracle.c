@@ -222,3 +222,37 @@ int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, 
     free(buf);
     return 0;
 }
+
+int dsa_oracle_oproj(const double* a_f64, const uint16_t* a_bf16, const uint16_t* w, int R, int K,
+                     int d_out, double* out, double* abs_out, int threads) {
+    if (R < 0 || K < 1 || d_out < 1 || !w || !out) return 1;
+    if ((a_f64 == NULL) == (a_bf16 == NULL)) return 1;
+    int nt = threads;
+#ifdef _OPENMP
+    if (nt <= 0) nt = omp_get_max_threads();
+#else
+    nt = 1;
+#endif
+    int r;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (r = 0; r < R; ++r) {
+        double* o = out + (size_t)r * (size_t)d_out;
+        double* ao = abs_out ? abs_out + (size_t)r * (size_t)d_out : NULL;
+        int n, k;
+        for (n = 0; n < d_out; ++n) {
+            o[n] = 0.0;
+            if (ao) ao[n] = 0.0;
+        }
+        for (k = 0; k < K; ++k) {
+            const size_t ak = (size_t)r * (size_t)K + (size_t)k;
+            const double a = a_f64 ? a_f64[ak] : widen_bf16(a_bf16[ak]);
+            const uint16_t* wk = w + (size_t)k * (size_t)d_out;
+            for (n = 0; n < d_out; ++n) {
+                const double wv = widen_bf16(wk[n]);
+                o[n] += a * wv;
+                if (ao) ao[n] += fabs(a) * fabs(wv);
+            }
+        }
+    }
+    return 0;
+}

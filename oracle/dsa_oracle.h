@@ -95,6 +95,22 @@ int dsa_oracle_max_threads(void);
 int dsa_oracle_topk(const float* scores, int ld, const int32_t* n_valid, int R, int k,
                     int k_max, int32_t* idx, int32_t* n_sel, int32_t* bad);
 
+/*
+ * Output projection, the step after the attention: a row's heads' outputs,
+ * concatenated (k = h*512 + c), times the projection matrix (TensorFold PR
+ * #1206, "What changes": the attention's output groups go to the output
+ * projections; the pages give no shape for the matrix, so d_out is the
+ * caller's):
+ *   out[r][n] = sum_{k<K} a[r][k] * w[k][n]          (summed in order k)
+ * a [R][K] is given either as doubles (a_f64, e.g. dsa_oracle_attn's output
+ * with K = H*512) or as bf16 bit patterns (a_bf16); exactly one is non-null.
+ * w [K][d_out] bf16 bit patterns.  out [R][d_out] double.  abs_out (may be
+ * null) receives sum_k |a[r][k]| * |w[k][n]|, the scale of a rounding bound.
+ * Returns 0, or 1 on an invalid argument.
+ */
+int dsa_oracle_oproj(const double* a_f64, const uint16_t* a_bf16, const uint16_t* w, int R, int K,
+                     int d_out, double* out, double* abs_out, int threads);
+
 #ifdef __cplusplus
 }
 #endif

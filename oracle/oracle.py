@@ -58,6 +58,8 @@ def load():
             lib.dsa_oracle_max_threads.restype = I
             lib.dsa_oracle_topk.argtypes = [P, I, P, I, I, I, P, P, P]
             lib.dsa_oracle_topk.restype = I
+            lib.dsa_oracle_oproj.argtypes = [P, P, P, I, I, I, P, P, I]
+            lib.dsa_oracle_oproj.restype = I
             _lib = lib
     return _lib
 
@@ -141,3 +143,30 @@ def topk(scores, n_valid, k: int, k_max: int = None):
     if rc:
         raise ValueError("oracle rejected its arguments")
     return idx, n_sel, bad
+
+
+def oproj(a, w_bf16, threads: int = 0):
+    """Output projection out = a . w (see dsa_oracle.h): ``a`` [R, K] as float64
+    (e.g. attention outputs reshaped to [R, H*512]) or as bf16 bit patterns
+    (uint16); ``w_bf16`` [K, d_out] bf16 bit patterns.  Returns (out float64
+    [R, d_out], abs float64 [R, d_out] = sum_k |a||w|)."""
+    lib = load()
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    if w.ndim != 2:
+        raise ValueError("w must be [K, d_out]")
+    K, d_out = w.shape
+    a = np.ascontiguousarray(a)
+    R = a.shape[0]
+    if a.size != R * K:
+        raise ValueError("a must be [rows, K]")
+    out = np.empty((R, d_out), np.float64)
+    absv = np.empty((R, d_out), np.float64)
+    if a.dtype == np.float64:
+        rc = lib.dsa_oracle_oproj(_ptr(a), None, _ptr(w), R, K, d_out, _ptr(out), _ptr(absv), threads)
+    elif a.dtype == np.uint16:
+        rc = lib.dsa_oracle_oproj(None, _ptr(a), _ptr(w), R, K, d_out, _ptr(out), _ptr(absv), threads)
+    else:
+        raise TypeError("a must be float64 or bf16 bit patterns (uint16)")
+    if rc:
+        raise ValueError("oracle rejected its arguments")
+    return out, absv

@@ -110,6 +110,41 @@ def test_topk_host_validation_before_any_launch(lib):
     assert call(R=0, scores=0) == dsa.DSA_OK
 
 
+def test_general_call_and_projection_host_validation(lib):
+    def attn(**kw):
+        a = dict(q=FAKE, kv=FAKE, idx=FAKE, n_sel=FAKE, sink=FAKE, out=FAKE, R=4, T=0, out_dtype=dsa.DSA_BF16)
+        a.update(kw)
+        return lib.dsa_sparse_attn(a["q"], a["kv"], a["idx"], a["n_sel"], a["sink"], 0.1, a["out"], a["R"],
+                                   a["T"], 64, 100, 8, dsa.DSA_BF16, a["out_dtype"], None)
+    assert attn(T=3) == dsa.DSA_ERR_INVALID_ARG                # rows not a multiple of rows_per_slot
+    assert attn(T=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(out_dtype=7) == dsa.DSA_ERR_UNSUPPORTED
+    assert attn(out=FAKE + 2) == dsa.DSA_ERR_INVALID_ARG       # misaligned out
+    assert attn(R=0, q=0, out=0) == dsa.DSA_OK
+
+    def proj(**kw):
+        a = dict(attn=FAKE, w=FAKE, out=FAKE, R=4, K=512, d_out=64)
+        a.update(kw)
+        return lib.dsa_oproj(a["attn"], a["w"], a["out"], a["R"], a["K"], a["d_out"], None)
+    for ptr in ("attn", "w", "out"):
+        assert proj(**{ptr: 0}) == dsa.DSA_ERR_INVALID_ARG
+    assert proj(K=0) == dsa.DSA_ERR_INVALID_ARG
+    assert proj(K=12) == dsa.DSA_ERR_INVALID_ARG               # not a multiple of 8
+    assert proj(d_out=6) == dsa.DSA_ERR_INVALID_ARG
+    assert proj(w=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG
+    assert proj(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert proj(R=0, attn=0, w=0, out=0) == dsa.DSA_OK
+
+    def fused(**kw):
+        a = dict(w=FAKE, attn=FAKE, out=FAKE, d_out=64)
+        a.update(kw)
+        return lib.dsa_sparse_attn_prefill_oproj(FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, a["w"], a["attn"], a["out"],
+                                                 4, 64, 100, 8, a["d_out"], None)
+    assert fused(w=0) == dsa.DSA_ERR_INVALID_ARG
+    assert fused(attn=0) == dsa.DSA_ERR_INVALID_ARG
+    assert fused(d_out=4) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_decode_rows_host_validation(lib):
     def call(B=2, T=2, **kw):
         a = dict(q=FAKE, kv=FAKE, idx=FAKE, n_sel=FAKE, sink=FAKE, out=FAKE)
