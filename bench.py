@@ -332,6 +332,34 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
     return sum(ms) / reps, c.R
 
 
+def bench_decode_rows(args, world, rank, local):
+    """Decode with T = --rows-per-slot rows a slot alone (for profiling): one
+    JSON line with its time and the KV bytes it selects, in total and as
+    distinct rows of each slot (the rows of a slot share most of their picks)."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    T = max(1, args.rows_per_slot)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    t_ms, rows = decode_rows_timing(dsa, dev, flush, T=T, reps=max(1, args.steps))
+    c = I.multi_row_decode(B=DEC_B, T=T, N=DEC_N)
+    distinct = 0
+    for b in range(DEC_B):
+        picks = set()
+        for r in range(b * T, (b + 1) * T):
+            picks.update(c.idx[r][:c.n_sel[r]].tolist())
+        distinct += len(picks)
+    if rank == 0:
+        print(json.dumps({"metric": "decode with %d rows a slot, ms per call" % T, "ms": t_ms, "rows": rows,
+                          "selected_kv_bytes": int(c.n_sel.astype(np.int64).sum()) * D * 2,
+                          "distinct_kv_bytes": distinct * D * 2}), flush=True)
+
+
 def bench_topk(args, world, rank, local):
     """The top-k selection alone (for profiling): prints one JSON line with
     the prefill-row and decode-row timings that the default run reports."""
@@ -700,9 +728,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk"), default="both",
-                    help="both (the benchmark step), one half of it for profiling, or the top-k "
-                         "selection alone")
+    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk", "decode_rows"), default="both",
+                    help="both (the benchmark step), one half of it for profiling, the top-k "
+                         "selection alone, or decode with --rows-per-slot rows a slot alone")
+    ap.add_argument("--rows-per-slot", type=int, default=2,
+                    help="rows a slot of the decode_rows workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
@@ -711,6 +741,8 @@ def main(argv=None):
         bench_reference(args, world, rank)
     elif args.workload == "topk":
         bench_topk(args, world, rank, local)
+    elif args.workload == "decode_rows":
+        bench_decode_rows(args, world, rank, local)
     else:
         bench_ours(args, world, rank, local)
 
