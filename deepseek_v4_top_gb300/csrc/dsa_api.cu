@@ -199,8 +199,10 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
     if (static_cast<long long>(R) * ((k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys) > (1LL << 30))
         return DSA_ERR_INVALID_ARG;
     if (dtype == DSA_F32 && R > 65535) return DSA_ERR_UNSUPPORTED;
-    // the kernels index q rows, and a decode batch's cache rows, with int32
-    if ((decode && static_cast<long long>(R) * N >= (1LL << 31)) || static_cast<long long>(R) * H >= (1LL << 31))
+    // the TMA map of q counts its rows (R * H) in int32; a decode batch's
+    // cache holds R / T slots of N rows (decode = T rows a slot)
+    if ((decode && static_cast<long long>(R / decode) * N >= (1LL << 31)) ||
+        static_cast<long long>(R) * H >= (1LL << 31))
         return DSA_ERR_INVALID_ARG;
     return DSA_OK;
 }
@@ -450,6 +452,7 @@ dsa_status dsa_shutdown(void) {
         ds = dsa::DeviceState();
     }
     if (have_cur) cudaSetDevice(cur);
+    dsa::noalloc_forget();
     return st;
 }
 

@@ -96,4 +96,10 @@ cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
 
+// Drops the cached device addresses of the no-allocation decode's static
+// array (dsa_noalloc.cu), so that the next call looks them up again: after
+// dsa_shutdown() the caller may reset the device, which reloads the module
+// and can move the array.
+void noalloc_forget();
+
 }  // namespace dsa

@@ -67,6 +67,12 @@ dsa_status noalloc_setup(NoAllocDevice** out) {
 }
 
 }  // namespace
+
+void noalloc_forget() {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    for (int d = 0; d < kNoAllocMaxDevices; ++d) g_na[d] = NoAllocDevice();
+}
+
 }  // namespace dsa
 
 extern "C" dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_cache,

@@ -227,8 +227,16 @@ DSA_API dsa_status dsa_sparse_attn_prefill_oproj(const void* q, const void* kv_c
  * - Every call uses the same array and it keeps the last call's contents:
  *   calls whose work overlaps on the GPU (other streams, other threads) race
  *   and corrupt each other's results.  Order them on one stream.
- * - Out-of-range selections still give NaN rows, but their error bits are not
- *   reported through dsa_get_device_error().
+ * - Device errors are not reported: this entry point has its own error word
+ *   in the static array, cleared at the start of every call and never read
+ *   back, so none of its bits (DSA_DEVERR_IDX_RANGE, DSA_DEVERR_NSEL_RANGE,
+ *   DSA_DEVERR_TIMEOUT, DSA_DEVERR_LAYOUT) reaches dsa_get_device_error().
+ *   Out-of-range selections still give NaN rows.  A call whose bounded wait
+ *   gave up, or that found its shared memory misaligned, leaves its outputs
+ *   undefined with no signal; callers that need that signal use
+ *   dsa_sparse_attn_decode().
+ * - dsa_shutdown() forgets the array's looked-up address, so a call after a
+ *   device reset looks it up again.
  */
 DSA_API dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_cache,
                                                   const int32_t* idx, const int32_t* n_sel,

@@ -52,21 +52,10 @@ def test_batched_decode_full_size():
     _check_full(I.batched_decode())
 
 
-def test_prefill_full_size_sampled():
-    """2048 rows at positions 2048..4095: all outputs finite; sampled
-    (row, head) pairs, spread over the persistent schedule, against the oracle."""
-    c = I.prefill()
-    got, code = run(c)
-    assert code == 0
-    assert np.isfinite(got).all()
-    rng = np.random.default_rng(4)
-    rows = np.concatenate([[0, 1, 151, 152, 303, 304, 1024, 2046, 2047],
-                           rng.integers(0, c.R, 23)]).astype(np.int32)
-    heads = rng.integers(0, c.H, len(rows)).astype(np.int32)
-    heads[:4] = [0, 63, 31, 32]
-    ref, _ = oracle.pairs(c, rows, heads)
-    sub = got[rows, heads][:, None, :]
-    compare(c, sub, ref[:, None, :])
+def test_prefill_full_size_every_pair():
+    """2048 rows at positions 2048..4095 of a 4096-position cache, k = 640:
+    every (row, head) output against the oracle (131,072 pairs)."""
+    _check_full(I.prefill())
 
 
 @pytest.mark.parametrize("first_pos,rows,N", [(0, 131, 512), (560, 90, 1024)])
@@ -115,14 +104,31 @@ def test_exact_sums_at_k640(mode):
             assert np.all(np.abs(got[r, h] - exact) <= ulp), (r, h)
 
 
-def test_five_repeats_are_bit_identical():
-    for c in (I.single_decode(), I.prefill(rows=200, N=2048, first_pos=1500)):
-        d = to_device(c)
-        first, _ = run(c, d)
-        for _ in range(4):
-            again, code = run(c, d)
-            assert code == 0
-            assert np.array_equal(first.view(np.uint32), again.view(np.uint32))
+_REPEAT_CASES = {
+    "single_decode_bf16": lambda: I.single_decode(),
+    "prefill_200_bf16": lambda: I.prefill(rows=200, N=2048, first_pos=1500),
+    "tiny_decode_fp32": lambda: I.tiny(mode="decode"),
+    "tiny_prefill_fp32": lambda: I.tiny(mode="prefill"),
+    "batched_decode_b8_full_size": lambda: I.batched_decode(),
+}
+for _j, _name in enumerate(I.EDGE_SPECIALS):
+    _REPEAT_CASES["special_" + _name] = (lambda n=_name, j=_j: I.edge_special(n, (I.SEED_BASE + 4) * 131 + j))
+
+
+@pytest.mark.parametrize("name", sorted(_REPEAT_CASES))
+def test_five_repeats_are_bit_identical(name):
+    """Five calls on the same inputs give the same bytes (akol1 TensorFold
+    PR #4, second commit message: five byte-identical repeats), on both
+    kernels (fp32 and bf16), through the split decode with its combine step,
+    and for every nonfinite special case of the edge sweep."""
+    c = _REPEAT_CASES[name]()
+    d = to_device(c)
+    first, code = run(c, d)
+    assert code == 0
+    for _ in range(4):
+        again, code = run(c, d)
+        assert code == 0
+        assert np.array_equal(first.view(np.uint32), again.view(np.uint32))
 
 
 def test_rows_do_not_depend_on_their_batch():

@@ -5,9 +5,11 @@ reserve all of it at start-up and forbid allocation afterwards, and callers
 on a latency-critical path where cudaMalloc / cudaFree would synchronise the
 device.  dsa_sparse_attn_decode_noalloc() serves them from a fixed static
 device array.  These tests call it through the C ABI and check it against
-dsa_sparse_attn_decode(), which allocates its scratch, on two calls in a
-row with different shapes, so a call cannot lean on what the one before it
-left in the shared array.  This file is collected last on purpose.
+dsa_sparse_attn_decode(), which allocates its scratch.  Both run the same
+kernels with the same key chunking, so the outputs must be the same bytes.
+Calls follow one another with different shapes, so a call cannot lean on
+what the one before it left in the shared array.  This file is collected
+last on purpose.
 """
 
 import numpy as np
@@ -19,6 +21,7 @@ from gpu_helpers import compare, to_device
 
 pytestmark = pytest.mark.gpu
 
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     import __graft_entry__
@@ -26,6 +29,7 @@ def _built():
     import torch
     assert torch.cuda.is_available()
     torch.cuda.set_device(0)
+
 
 def _call(name, case, d):
     """One decode call through the C ABI with raw device addresses."""
@@ -40,16 +44,59 @@ def _call(name, case, d):
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
-def test_noalloc_decode_matches_the_allocating_decode_twice_in_a_row():
-    first = I.batched_decode(B=8, N=8192)                 # 8 rows x 5 chunks = 40 units
+
+def _both(case):
+    """The allocating decode, its device error word, then the no-allocation
+    decode on the same device inputs."""
+    from deepseek_v4_top_gb300 import dsa
+    d = to_device(case)
+    ref = _call("dsa_sparse_attn_decode", case, d)
+    code = dsa.dsa_get_device_error()
+    got = _call("dsa_sparse_attn_decode_noalloc", case, d)
+    assert dsa.dsa_get_device_error() == 0     # this entry point reports no error bits
+    return ref, code, got
+
+
+def _cases():
     rng = np.random.default_rng(12)
-    second = I._edge_base(rng, "second", I.BF16, 32, 300, "decode", R=3, N=2000, k_extra=20)
-    for case in (first, second):
-        d = to_device(case)
-        ref = _call("dsa_sparse_attn_decode", case, d).astype(np.float64)
-        got = _call("dsa_sparse_attn_decode_noalloc", case, d)
-        assert np.isfinite(got).all()
-        compare(case, got, ref)
+    return [
+        # 8 rows x 5 key chunks = 40 units: partials and the combine step
+        I.batched_decode(B=8, N=8192),
+        # ragged rows over three chunks of up to 128 keys
+        I._edge_base(rng, "three_chunks", I.BF16, 32, 300, "decode", R=3, N=2000, k_extra=20),
+        # k_max <= 128: one chunk a row, written straight to the output
+        I._edge_base(rng, "one_chunk", I.BF16, 64, 100, "decode", R=5, N=1500, k_extra=28),
+        # exactly DSA_NOALLOC_MAX_UNITS units: 8 rows x ceil(1024 / 128)
+        I._edge_base(rng, "max_units", I.BF16, 64, 1024, "decode", R=8, N=3000, k_extra=0),
+    ]
+
+
+def test_noalloc_decode_is_bit_identical_to_the_allocating_decode_call_after_call():
+    from deepseek_v4_top_gb300 import dsa
+    cases = _cases()
+    assert cases[3].R * -(-cases[3].k_max // 128) == dsa.DSA_NOALLOC_MAX_UNITS
+    for case in cases:
+        ref, code, got = _both(case)
+        assert code == 0
+        assert np.isfinite(got).all(), case.name
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), case.name
+        compare(case, got, ref.astype(np.float64))
+
+
+def test_noalloc_out_of_range_selection_gives_a_nan_row():
+    """A selected index >= N makes that row NaN (the error bit is lost on this
+    entry point); the other rows are the allocating decode's bytes."""
+    from deepseek_v4_top_gb300 import dsa
+    rng = np.random.default_rng(13)
+    case = I._edge_base(rng, "bad_index", I.BF16, 64, 400, "decode", R=4, N=2500, k_extra=0)
+    case.idx[2, 150] = case.N
+    ref, code, got = _both(case)
+    assert code == dsa.DSA_DEVERR_IDX_RANGE
+    assert np.isnan(got[2]).all()
+    for r in (0, 1, 3):
+        assert np.isfinite(got[r]).all()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
 
 def test_noalloc_rejects_batches_beyond_its_fixed_scratch():
     from deepseek_v4_top_gb300 import dsa
