@@ -703,6 +703,93 @@ def bench_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------ head-sharded (TP)
+def bench_tp(args, world, rank, local):
+    """The benchmark step with the 64 heads split over the ranks (TensorFold
+    PR #1206: 16 heads a rank at world 4): each rank runs the decode and
+    prefill calls over its heads, NCCL all-gathers the outputs and the
+    library lays them out as [rows, 64, 512].  Total work is fixed, so the
+    scaling is strong.  q is cut into the ranks' heads once, before timing
+    (a model's sharded q projection would produce it so)."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    plan = dsa.dsa_head_shard(H, world, rank)
+    hpr = plan.heads_per_rank
+    work = []
+    for case, T in ((I.batched_decode(B=DEC_B, N=DEC_N), 1), (I.prefill(rows=PRE_R, N=PRE_N), 0)):
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        d = dict(q=up(case.q), kv=up(case.kv), idx=torch.from_numpy(case.idx).to(dev),
+                 n_sel=torch.from_numpy(case.n_sel).to(dev), sink=torch.from_numpy(case.sink).to(dev))
+        ql = torch.empty((case.R, hpr, D), dtype=torch.bfloat16, device=dev)
+        sl = torch.empty((hpr,), dtype=torch.float32, device=dev)
+        dsa.dsa_shard_heads(d["q"], d["sink"], ql, sl, world, rank)
+        work.append(dict(case=case, T=T, d=d, ql=ql, sl=sl,
+                         ol=torch.empty((case.R, hpr, D), dtype=torch.float32, device=dev),
+                         g=torch.empty((world, case.R, hpr, D), dtype=torch.float32, device=dev),
+                         out=torch.empty((case.R, H, D), dtype=torch.float32, device=dev)))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for w in work:
+            dsa.tp_sparse_attn(w["ql"], w["d"]["kv"], w["d"]["idx"], w["d"]["n_sel"], w["sl"], w["case"].scale,
+                               w["ol"], w["g"], w["out"], rows_per_slot=w["T"])
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    hold_gpu(stream)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    clocks.stop()
+    step_ms = reduce_max(sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps, world)
+    assert dsa.dsa_get_device_error() == 0
+    for w in work:
+        assert torch.isfinite(w["out"]).all().item()
+    units = (DEC_B + PRE_R) * H
+    line = {
+        "metric": METRIC, "value": units / (step_ms * 1e-3), "unit": "row*heads/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/kv, seeded distinct and causal top-k indices)",
+        "config": {"workload": WORKLOAD, "decode": {"B": DEC_B, "N": DEC_N}, "prefill": {"rows": PRE_R, "N": PRE_N},
+                   "heads": H, "heads_per_rank": hpr, "d": D, "k": K,
+                   "parallelism": "tp%d (heads split over ranks; NCCL all-gather of the outputs)" % world,
+                   "l2": "flushed before every step by writing 2x L2; events bracket the calls only"},
+        "gpu_launches": 5 * args.steps,      # decode: split + combine + unshard; prefill: attention + unshard
+        "clocks": clocks.summary(t0, t1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------- reference
 def bench_reference(args, world, rank):
     """The fp64 CPU oracle, as it stands, on the host cores (rank 0 only)."""
@@ -766,6 +853,9 @@ def main(argv=None):
                          "selection alone, or decode with --rows-per-slot rows a slot alone")
     ap.add_argument("--rows-per-slot", type=int, default=2,
                     help="rows a slot of the decode_rows workload")
+    ap.add_argument("--tp", action="store_true",
+                    help="split the 64 heads over the ranks (head-sharded tensor parallelism) instead of "
+                         "running independent replicas")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
@@ -776,6 +866,8 @@ def main(argv=None):
         bench_topk(args, world, rank, local)
     elif args.workload == "decode_rows":
         bench_decode_rows(args, world, rank, local)
+    elif args.tp:
+        bench_tp(args, world, rank, local)
     else:
         bench_ours(args, world, rank, local)
 

@@ -34,12 +34,18 @@ DSA_DEVERR_NVALID_RANGE = 0x10
 EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_decode_rows", "dsa_sparse_attn_prefill",
            "dsa_sparse_attn", "dsa_oproj", "dsa_sparse_attn_prefill_oproj",
            "dsa_sparse_attn_decode_noalloc",
-           "dsa_topk_select", "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string",
-           "dsa_shutdown")
+           "dsa_topk_select", "dsa_head_shard", "dsa_shard_heads", "dsa_unshard_heads",
+           "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
 DSA_NOALLOC_MAX_UNITS = 64
 
 _lib = None
 _lock = threading.Lock()
+
+
+class HeadShardPlan(ctypes.Structure):
+    """dsa_head_shard_plan of include/dsa.h."""
+    _fields_ = [("heads_per_rank", ctypes.c_int), ("padded_heads", ctypes.c_int),
+                ("first_head", ctypes.c_int), ("real_heads", ctypes.c_int)]
 
 
 class DsaError(RuntimeError):
@@ -73,6 +79,12 @@ def load():
             lib.dsa_sparse_attn_prefill_oproj.restype = I
             lib.dsa_topk_select.argtypes = [P, I, P, I, I, P, I, P, P]
             lib.dsa_topk_select.restype = I
+            lib.dsa_head_shard.argtypes = [I, I, I, ctypes.POINTER(HeadShardPlan)]
+            lib.dsa_head_shard.restype = I
+            lib.dsa_shard_heads.argtypes = [P, P, P, P, I, I, I, I, I, P]
+            lib.dsa_shard_heads.restype = I
+            lib.dsa_unshard_heads.argtypes = [P, P, I, I, I, I, P]
+            lib.dsa_unshard_heads.restype = I
             lib.dsa_selftest_wait_limit.argtypes = [P]
             lib.dsa_selftest_wait_limit.restype = I
             lib.dsa_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -276,6 +288,80 @@ def dsa_topk_select(scores, n_valid, k, idx, n_sel, stream=None):
     if st != DSA_OK:
         raise DsaError(st, "dsa_topk_select")
     return idx, n_sel
+
+
+# ------------------------------------------------- head-sharded parallelism
+def dsa_head_shard(H: int, world: int, rank: int) -> HeadShardPlan:
+    """Which heads rank `rank` of `world` owns (host only; see include/dsa.h)."""
+    plan = HeadShardPlan()
+    st = load().dsa_head_shard(int(H), int(world), int(rank), ctypes.byref(plan))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_head_shard")
+    return plan
+
+
+def dsa_shard_heads(q, sink, q_local, sink_local, world: int, rank: int, stream=None):
+    """q_local [R,hpr,512], sink_local [hpr] = rank's heads of q [R,H,512],
+    sink [H] (zero for padding heads)."""
+    import torch
+    for name, t in (("q", q), ("sink", sink), ("q_local", q_local), ("sink_local", sink_local)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if q.dim() != 3 or q.shape[2] != 512 or q_local.dtype != q.dtype:
+        raise ValueError("q [rows, heads, 512] and q_local of the same dtype expected")
+    R, H = q.shape[0], q.shape[1]
+    plan = dsa_head_shard(H, world, rank)
+    if tuple(q_local.shape) != (R, plan.heads_per_rank, 512) or tuple(sink.shape) != (H,) \
+            or tuple(sink_local.shape) != (plan.heads_per_rank,):
+        raise ValueError("q_local [rows, heads_per_rank, 512], sink [heads], sink_local [heads_per_rank] expected")
+    if sink.dtype != torch.float32 or sink_local.dtype != torch.float32:
+        raise TypeError("sinks must be float32")
+    st = load().dsa_shard_heads(q.data_ptr(), sink.data_ptr(), q_local.data_ptr(), sink_local.data_ptr(),
+                                R, H, int(world), int(rank), _dtype_code(q), _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_shard_heads")
+    return q_local, sink_local
+
+
+def dsa_unshard_heads(gathered, out, world: int, stream=None):
+    """out [R,H,512] from gathered [world,R,hpr,512] (padding heads dropped)."""
+    import torch
+    for name, t in (("gathered", gathered), ("out", out)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if out.dim() != 3 or out.shape[2] != 512 or gathered.dtype != out.dtype:
+        raise ValueError("out [rows, heads, 512] and gathered of the same dtype expected")
+    R, H = out.shape[0], out.shape[1]
+    plan = dsa_head_shard(H, world, 0)
+    if tuple(gathered.shape) != (world, R, plan.heads_per_rank, 512):
+        raise ValueError("gathered must be [world, rows, heads_per_rank, 512]")
+    st = load().dsa_unshard_heads(gathered.data_ptr(), out.data_ptr(), R, H, int(world), _dtype_code(out),
+                                  _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_unshard_heads")
+    return out
+
+
+def tp_sparse_attn(q_local, kv_cache, idx, n_sel, sink_local, scale, out_local, gathered, out, group=None,
+                   rows_per_slot=0, stream=None):
+    """One rank's step of head-sharded attention, all on one stream (torch's
+    current one unless `stream` is given): the attention call over the rank's
+    heads into out_local [R,hpr,512], an all-gather of every rank's out_local
+    into gathered [world,R,hpr,512] (torch.distributed on `group`; NCCL on
+    GPUs), then the gathered outputs laid out as out [R,H,512].  With one
+    rank, out_local itself is the gathered array."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
+    with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+        dsa_sparse_attn(q_local, kv_cache, idx, n_sel, sink_local, scale, out_local,
+                        rows_per_slot=rows_per_slot)
+        if world > 1:
+            dist.all_gather_into_tensor(gathered.view(-1), out_local.view(-1), group=group)
+            src = gathered
+        else:
+            src = out_local.view((1,) + tuple(out_local.shape))
+        return dsa_unshard_heads(src, out, world)
 
 
 def dsa_selftest_wait_limit(stream=None) -> None:

@@ -278,6 +278,55 @@ DSA_API dsa_status dsa_topk_select(const float* scores, int ld, const int32_t* n
                                    void* stream);
 
 /*
+ * Head-sharded tensor parallelism (TensorFold PR #1206, "What changes": the
+ * 64 heads are split over the ranks, 16 a rank at world 4; heads added to
+ * fill the last rank get zero sinks; the output groups are gathered before
+ * the output projections).  A rank runs the attention calls above over its
+ * own heads (H = heads_per_rank); the calls below plan the split, cut a
+ * rank's heads out of full arrays, and lay the gathered outputs back out.
+ * The gathering itself is the caller's collective (an all-gather of every
+ * rank's out [R][heads_per_rank][512], rank after rank).
+ *
+ * Plan for H heads over `world` ranks: heads_per_rank = ceil(H / world),
+ * padded_heads = heads_per_rank * world; rank w owns heads
+ * [first_head, first_head + heads_per_rank), of which the first real_heads
+ * are < H and the rest are padding.  Host only; no device is touched.
+ * DSA_ERR_INVALID_ARG for a null plan, H < 1, world < 1 or rank outside
+ * [0, world); DSA_ERR_UNSUPPORTED when heads_per_rank > 64.
+ */
+typedef struct {
+    int heads_per_rank;
+    int padded_heads;
+    int first_head;
+    int real_heads;
+} dsa_head_shard_plan;
+
+DSA_API dsa_status dsa_head_shard(int H, int world, int rank, dsa_head_shard_plan* plan);
+
+/*
+ * A rank's inputs from the full ones: q_local [R][heads_per_rank][512] and
+ * sink_local [heads_per_rank] take heads first_head.. of q [R][H][512] and
+ * sink [H]; a padding head gets q = 0 and sink = 0.  Values are copied bit
+ * for bit.  q and q_local (dtype: float32 or bf16) 16-byte aligned, device
+ * pointers; asynchronous on `stream`.  Errors as dsa_head_shard, plus
+ * DSA_ERR_INVALID_ARG for null or misaligned pointers or R < 0.
+ */
+DSA_API dsa_status dsa_shard_heads(const void* q, const float* sink, void* q_local, float* sink_local,
+                                   int R, int H, int world, int rank, dsa_dtype dtype, void* stream);
+
+/*
+ * The gathered outputs laid out as one call's: gathered
+ * [world][R][heads_per_rank][512] (rank after rank, as an all-gather of the
+ * ranks' out arrays leaves them) into out [R][H][512]; head h comes from
+ * rank h / heads_per_rank and padding heads are dropped.  Bit for bit.
+ * dtype is the outputs' (DSA_F32 or DSA_BF16); both pointers 16-byte
+ * aligned device pointers that do not overlap; asynchronous on `stream`.
+ * Errors as dsa_shard_heads.
+ */
+DSA_API dsa_status dsa_unshard_heads(const void* gathered, void* out, int R, int H, int world,
+                                     dsa_dtype dtype, void* stream);
+
+/*
  * Self-test of the bounded waits (the pages have no counterpart): queues on
  * `stream` one small kernel whose only wait is on a barrier that nothing
  * completes.  After the library's wait limit (about 2 seconds) the wait gives
