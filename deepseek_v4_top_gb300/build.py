@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
 SOURCES = ["dsa_api.cu", "dsa_tc.cu", "dsa_simt.cu", "dsa_noalloc.cu", "dsa_topk.cu", "dsa_selftest.cu",
            "dsa_tp.cu"]
-HEADERS = ["dsa_internal.h", "dsa_ptx.cuh"]
+HEADERS = ["dsa_internal.h", "dsa_ptx.cuh", "dsa_merge.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", os.path.join(ROOT, "include")]

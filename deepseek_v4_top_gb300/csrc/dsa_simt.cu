@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "dsa_internal.h"
+#include "dsa_merge.cuh"
 #include "dsa_ptx.cuh"
 
 namespace dsa {
@@ -20,7 +21,6 @@ namespace {
 
 constexpr int kSimtThreads = 128;
 constexpr int kSimtTile = 16;
-constexpr float kLog2e = 1.4426950408889634f;
 
 #define DSA_R8(x) x, x, x, x, x, x, x, x
 #define DSA_R64(x) DSA_R8(DSA_R8(x))
@@ -122,9 +122,8 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
 }
 
 // One CTA per (row, head); thread t owns columns 4t .. 4t+3.  Partials of
-// one row are merged in chunk order, so the result is deterministic.  Each
-// partial holds (m, l, O) with O and l relative to 2^m (2^0 when m is -inf,
-// in which case O and l are 0 or NaN).
+// one row are merged in chunk order (dsa_merge.cuh), so the result is
+// deterministic and the same as the merge inside the tensor-core kernel.
 __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p) {
     grid_launch_dependents();
     grid_dependency_wait();          // the split kernel's partials are complete
@@ -132,56 +131,82 @@ __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p)
     const int tid = threadIdx.x;
     const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
     const size_t u0 = static_cast<size_t>(r) * p.chunks;
-    // Chunks are taken kBatch at a time, all loads of a batch issued before
-    // any of them is used; the arithmetic runs in chunk order.
+    // Up to kBatch chunks: every load (m, l and this thread's float4 of O for
+    // each chunk) is issued at once, then the maximum, then the sums in chunk
+    // order.  More chunks: a first pass over m for the maximum, then the
+    // chunks kBatch at a time.  Both give the same arithmetic.
     constexpr int kBatch = 8;
     float M = -INFINITY;
     bool have = false;
-    for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
-        float mv[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j)
-            mv[j] = c0 + j < p.chunks ? ml_base[(u0 + c0 + j) * 2 * kHeadsPad + h] : -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            if (mv[j] != -INFINITY) {
-                M = have ? fmaxf(M, mv[j]) : mv[j];
-                have = true;
-            }
-        }
-    }
-    const float mu = have ? M : 0.0f;
     float l = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
+    if (p.chunks <= kBatch) {
         float mv[kBatch], lv[kBatch];
         float4 ov[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            if (c0 + j < p.chunks) {
-                const size_t u = u0 + c0 + j;
+            if (j < p.chunks) {
+                const size_t u = u0 + j;
                 mv[j] = ml_base[u * 2 * kHeadsPad + h];
                 lv[j] = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
                 ov[j] = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
+            } else {
+                mv[j] = -INFINITY;
             }
         }
 #pragma unroll
+        for (int j = 0; j < kBatch; ++j) merge_max(M, have, mv[j]);
+        const float mu = merge_ref(M, have);
+#pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            if (c0 + j < p.chunks) {
-                const float w = (mv[j] == -INFINITY) ? 1.0f : exp2f(mv[j] - mu);
-                l += w * lv[j];
+            if (j < p.chunks) {
+                const float w = merge_weight(mv[j], mu);
+                l = fmaf(w, lv[j], l);
                 acc.x = fmaf(w, ov[j].x, acc.x);
                 acc.y = fmaf(w, ov[j].y, acc.y);
                 acc.z = fmaf(w, ov[j].z, acc.z);
                 acc.w = fmaf(w, ov[j].w, acc.w);
             }
         }
+        M = mu;
+    } else {
+        for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
+            float mv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                mv[j] = c0 + j < p.chunks ? ml_base[(u0 + c0 + j) * 2 * kHeadsPad + h] : -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) merge_max(M, have, mv[j]);
+        }
+        const float mu = merge_ref(M, have);
+        for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
+            float mv[kBatch], lv[kBatch];
+            float4 ov[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (c0 + j < p.chunks) {
+                    const size_t u = u0 + c0 + j;
+                    mv[j] = ml_base[u * 2 * kHeadsPad + h];
+                    lv[j] = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
+                    ov[j] = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (c0 + j < p.chunks) {
+                    const float w = merge_weight(mv[j], mu);
+                    l = fmaf(w, lv[j], l);
+                    acc.x = fmaf(w, ov[j].x, acc.x);
+                    acc.y = fmaf(w, ov[j].y, acc.y);
+                    acc.z = fmaf(w, ov[j].z, acc.z);
+                    acc.w = fmaf(w, ov[j].w, acc.w);
+                }
+            }
+        }
+        M = mu;
     }
-    const float s2 = p.sink[h] * kLog2e;
-    const float mstar = isfinite(s2) ? fmaxf(mu, s2) : mu;
-    const float e1 = exp2f(mu - mstar);
-    const float e2 = exp2f(s2 - mstar);
-    const float f = e1 / (l * e1 + e2);
+    const float mu = M;
+    const float f = merge_factor(mu, l, p.sink[h]);
     const float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
     const size_t o0 = (static_cast<size_t>(r) * p.H + h) * kD;
     if (p.out_bf16) {
