@@ -291,10 +291,11 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
 
 def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
     """The prefill rows' attention with a bf16 output, then their output
-    projection (out [2048, d_out] fp32 = attn [2048, 64*512] bf16 . w_o), each
-    call alone with the L2 flushed before it.  w_o is seeded N(0, 1/K) on the
-    device (the pages give no projection weights or width).  Returns (attention
-    ms, projection ms)."""
+    projection (out [2048, d_out] fp32 = attn [2048, 64*512] bf16 . w_o) by
+    the library's GEMM, and, for comparison, the same product by cuBLAS
+    (torch.matmul, bf16 out), each call alone with the L2 flushed before it.
+    w_o is seeded N(0, 1/K) on the device (the pages give no projection
+    weights or width).  Returns (attention ms, projection ms, cuBLAS ms)."""
     import torch
     K = H * D
     g = torch.Generator(device=dev)
@@ -302,6 +303,7 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
     w_o = (torch.randn((K, d_out), generator=g, device=dev) * K ** -0.5).to(torch.bfloat16)
     attn = torch.empty((PRE_R, H, D), dtype=torch.bfloat16, device=dev)
     out = torch.empty((PRE_R, d_out), dtype=torch.float32, device=dev)
+    ref = torch.empty((PRE_R, d_out), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
     def call_attn():
@@ -311,8 +313,11 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
     def call_proj():
         dsa.dsa_oproj(attn, w_o, out, stream)
 
+    def call_cublas():
+        torch.matmul(attn.view(PRE_R, K), w_o, out=ref)
+
     res = []
-    for fn in (call_attn, call_proj):
+    for fn in (call_attn, call_proj, call_cublas):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -327,7 +332,7 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
         res.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps)
     assert dsa.dsa_get_device_error() == 0
     assert torch.isfinite(out).all().item()
-    return res[0], res[1]
+    return res[0], res[1], res[2]
 
 
 def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
@@ -601,8 +606,8 @@ def bench_ours(args, world, rank, local):
                 "how": "dsa_topk_select, k=%d, N(0,1) scores, one call a time, L2 flushed before each" % K}
     if do_pre:
         # the prefill rows with a bf16 output, then their output projection
-        a_ms, p_ms = oproj_timing(dsa, dev, flush, d_pre, pre)
-        a_ms, p_ms = reduce_max(a_ms, world), reduce_max(p_ms, world)
+        a_ms, p_ms, c_ms = oproj_timing(dsa, dev, flush, d_pre, pre)
+        a_ms, p_ms, c_ms = reduce_max(a_ms, world), reduce_max(p_ms, world), reduce_max(c_ms, world)
         g = PRE_R * K * D * 2
         workloads["prefill_2048_bf16_out"] = {
             "ms": a_ms, "row_heads_per_s": PRE_R * H / (a_ms * 1e-3),
@@ -616,8 +621,12 @@ def bench_ours(args, world, rank, local):
             "frac_note": "denominator: MEASURED_PEAKS.json bf16_tflops, a best-of-10 torch.matmul "
                          "8192^3 rate on this GPU (not a hardware peak; the nominal dense bf16 peak "
                          "is 2250 TFLOP/s)",
-            "how": "dsa_oproj (cuBLASLt, bf16 x bf16 -> fp32): the 2048 rows' bf16 attention output times a "
-                   "seeded [32768, %d] bf16 projection, one call a time, L2 flushed before each" % OPROJ_D_OUT}
+            "cublas_ms": c_ms, "cublas_tflops": p_flops / (c_ms * 1e-3) / 1e12,
+            "time_vs_cublas": c_ms / p_ms,
+            "how": "dsa_oproj (the library's tcgen05 GEMM, bf16 x bf16 -> fp32): the 2048 rows' bf16 attention "
+                   "output times a seeded [32768, %d] bf16 projection, one call a time, L2 flushed before each; "
+                   "cublas_ms: torch.matmul of the same operands (cuBLAS, bf16 out), timed the same way, for "
+                   "comparison only" % OPROJ_D_OUT}
     roofline = None
     if do_pre:
         g = PRE_R * K * D * 2

@@ -1,8 +1,7 @@
 """Builds libdsa.so in-tree with nvcc for sm_103a (no torch extension machinery).
 
 The CUDA translation units compile in parallel; the shared library links
-the CUDA runtime statically and cuBLASLt (the output projection's GEMM)
-dynamically, and exports only the C ABI of include/dsa.h.
+the CUDA runtime statically and exports only the C ABI of include/dsa.h.
 """
 
 from __future__ import annotations
@@ -18,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
 SOURCES = ["dsa_api.cu", "dsa_tc.cu", "dsa_simt.cu", "dsa_noalloc.cu", "dsa_topk.cu", "dsa_selftest.cu",
-           "dsa_tp.cu"]
+           "dsa_tp.cu", "dsa_gemm.cu"]
 HEADERS = ["dsa_internal.h", "dsa_ptx.cuh", "dsa_merge.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -66,7 +65,7 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-lcublasLt", "-o", tmp]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

@@ -5,7 +5,6 @@
 
 #include <mutex>
 
-#include <cublasLt.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dsa.h"
@@ -25,8 +24,6 @@ struct DeviceState {
     size_t scratch_bytes = 0;
     void* topk_scratch = nullptr;  // two-step top-k: the shares' picks
     size_t topk_scratch_bytes = 0;
-    cublasLtHandle_t lt = nullptr;  // the output projection's GEMM
-    void* lt_work = nullptr;
     int sm_count = 0;
     cudaStream_t queue_stream[kQueues] = {};
     int queues_used = 0;
@@ -90,77 +87,6 @@ dsa_status ensure_scratch(DeviceState* st, size_t bytes, float** out) {
     const dsa_status r = ensure_buffer(reinterpret_cast<void**>(&st->scratch), &st->scratch_bytes, bytes, &v);
     *out = static_cast<float*>(v);
     return r;
-}
-
-// The output projection: out [R][d_out] fp32 = attn [R][K] bf16 . w_o [K][d_out]
-// bf16, accumulated in fp32 by cuBLASLt (a plain library GEMM).  Row-major
-// C = A.B is column-major C^T = B^T.A^T, so cuBLASLt sees m = d_out, n = R,
-// k = K with its A = w_o (ld d_out), its B = attn (ld K) and C = out (ld
-// d_out).  Only algorithms without a split-K reduction are taken, so a
-// call's result does not depend on the run.  The handle and a 32 MB
-// workspace are made once per device.
-constexpr size_t kLtWorkBytes = static_cast<size_t>(32) << 20;
-
-dsa_status oproj_gemm(DeviceState* ds, const void* attn, const void* w_o, float* out, int R, int K, int d_out,
-                      cudaStream_t s) {
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!ds->lt) {
-            if (cublasLtCreate(&ds->lt) != CUBLAS_STATUS_SUCCESS) {
-                ds->lt = nullptr;
-                return DSA_ERR_CUDA;
-            }
-            if (cudaMalloc(&ds->lt_work, kLtWorkBytes) != cudaSuccess) {
-                cublasLtDestroy(ds->lt);
-                ds->lt = nullptr;
-                ds->lt_work = nullptr;
-                return DSA_ERR_CUDA;
-            }
-        }
-    }
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
-    dsa_status st = DSA_ERR_CUDA;
-    do {
-        if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) break;
-        const cublasOperation_t no_t = CUBLAS_OP_N;
-        if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &no_t, sizeof(no_t)) !=
-                CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &no_t, sizeof(no_t)) !=
-                CUBLAS_STATUS_SUCCESS)
-            break;
-        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, d_out, K, d_out) != CUBLAS_STATUS_SUCCESS) break;
-        if (cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, K, R, K) != CUBLAS_STATUS_SUCCESS) break;
-        if (cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, d_out, R, d_out) != CUBLAS_STATUS_SUCCESS) break;
-        if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
-        const size_t ws = kLtWorkBytes;
-        const uint32_t no_split = CUBLASLT_REDUCTION_SCHEME_NONE;
-        if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws,
-                                                 sizeof(ws)) != CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &no_split,
-                                                 sizeof(no_split)) != CUBLAS_STATUS_SUCCESS)
-            break;
-        cublasLtMatmulHeuristicResult_t h = {};
-        int found = 0;
-        if (cublasLtMatmulAlgoGetHeuristic(ds->lt, op, la, lb, lc, lc, pref, 1, &h, &found) !=
-                CUBLAS_STATUS_SUCCESS ||
-            found == 0) {
-            st = DSA_ERR_UNSUPPORTED;
-            break;
-        }
-        const float one = 1.0f, zero = 0.0f;
-        if (cublasLtMatmul(ds->lt, op, &one, w_o, la, attn, lb, &zero, out, lc, out, lc, &h.algo, ds->lt_work,
-                           kLtWorkBytes, s) != CUBLAS_STATUS_SUCCESS)
-            break;
-        st = DSA_OK;
-    } while (false);
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return st;
 }
 
 // The row queue of stream s, or null (round-robin rows) when s may run on
@@ -330,7 +256,10 @@ dsa_status dsa_oproj(const void* attn, const void* w_o, float* out, int R, int K
     dsa::DeviceState* ds = nullptr;
     dsa_status st = dsa::device_state(&ds);
     if (st != DSA_OK) return st;
-    return dsa::oproj_gemm(ds, attn, w_o, out, R, K, d_out, static_cast<cudaStream_t>(stream));
+    return dsa::launch_gemm(attn, w_o, out, R, K, d_out, ds->err, ds->sm_count, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? DSA_OK
+               : DSA_ERR_CUDA;
 }
 
 dsa_status dsa_sparse_attn_prefill_oproj(const void* q, const void* kv_cache, const int32_t* idx,
@@ -439,7 +368,7 @@ dsa_status dsa_shutdown(void) {
     dsa_status st = DSA_OK;
     for (int d = 0; d < dsa::kMaxDevices; ++d) {
         dsa::DeviceState& ds = dsa::g_dev[d];
-        if (!ds.err && !ds.scratch && !ds.topk_scratch && !ds.lt) continue;
+        if (!ds.err && !ds.scratch && !ds.topk_scratch) continue;
         if (cudaSetDevice(d) != cudaSuccess) {
             st = DSA_ERR_CUDA;
             continue;
@@ -447,8 +376,6 @@ dsa_status dsa_shutdown(void) {
         if (ds.err) cudaFree(ds.err);
         if (ds.scratch) cudaFree(ds.scratch);
         if (ds.topk_scratch) cudaFree(ds.topk_scratch);
-        if (ds.lt_work) cudaFree(ds.lt_work);
-        if (ds.lt) cublasLtDestroy(ds.lt);
         ds = dsa::DeviceState();
     }
     if (have_cur) cudaSetDevice(cur);

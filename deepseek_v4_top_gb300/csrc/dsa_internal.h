@@ -95,6 +95,10 @@ cudaError_t launch_tc(const TcParams& p, int grid, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t s);
+// out [M][N] fp32 = a [M][K] bf16 . b [K][N] bf16 on the tensor cores
+// (dsa_gemm.cu); K and N multiples of 8, pointers 16-byte aligned.
+cudaError_t launch_gemm(const void* a, const void* b, float* out, int M, int K, int N, uint32_t* err, int sms,
+                        cudaStream_t s);
 
 // Drops the cached device addresses of the no-allocation decode's static
 // array (dsa_noalloc.cu), so that the next call looks them up again: after

@@ -173,14 +173,14 @@ DSA_API dsa_status dsa_sparse_attn(const void* q, const void* kv_cache,
  *        [R][H][512] bf16 out of dsa_sparse_attn),
  *   w_o  [K][d_out] bfloat16, row-major,
  *   out  [R][d_out] float32 = attn . w_o, accumulated in float32.
- * A plain GEMM, run by cuBLASLt (no split-K reduction, so repeated calls
- * give the same bits).  The pages give no shape for this projection;
- * d_out is the caller's.  All three 16-byte aligned, K and d_out multiples
- * of 8.  The first call on a device creates a cuBLASLt handle and a 32 MB
- * workspace, kept until dsa_shutdown(); calls whose work overlaps on the GPU
- * share that workspace and race: order them on one stream.
- * DSA_ERR_INVALID_ARG for null pointers or bad sizes, DSA_ERR_UNSUPPORTED if
- * cuBLASLt offers no algorithm, DSA_ERR_CUDA if it fails.
+ * Run by this library's own tensor-core kernel (tcgen05 MMAs fed by TMA, two
+ * TMEM accumulators; no split of K, so every output is one fp32 sum in a
+ * fixed order and repeated calls give the same bits).  The pages give no
+ * shape for this projection; d_out is the caller's.  All three 16-byte
+ * aligned, K and d_out multiples of 8.  Allocates nothing beyond the
+ * per-device error word.  A wait that gives up sets DSA_DEVERR_TIMEOUT
+ * (outputs undefined).  DSA_ERR_INVALID_ARG for null pointers or bad
+ * sizes, DSA_ERR_CUDA if the launch fails.
  */
 DSA_API dsa_status dsa_oproj(const void* attn, const void* w_o, float* out,
                              int R, int K, int d_out, void* stream);

@@ -4,8 +4,10 @@
   even, bit for bit, on every kernel path (tensor-core prefill, with and
   without the row queue; split decode and its combine; several rows a slot;
   the fp32-input kernel).
-- dsa_oproj against the oracle's fp64 product of the same bf16 inputs,
-  within the float32-accumulation bound K * 2^-24 * sum_k |a||w|.
+- dsa_oproj (the library's tensor-core GEMM) against the oracle's fp64
+  product of the same bf16 inputs, within the float32-accumulation bound
+  K * 2^-24 * sum_k |a||w|, on ragged tiles and on more tiles than SMs;
+  repeated calls give the same bits.
 - dsa_sparse_attn_prefill_oproj against the oracle's attention followed by
   the oracle's projection, within the bound that the attention's parity bar,
   the bf16 rounding and the accumulation give together.
@@ -78,7 +80,11 @@ def _bf16_bits(rng, shape, scale=1.0):
     return I.f32_to_bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
 
 
-@pytest.mark.parametrize("R,K,d_out", [(48, 4096, 256), (16, 32768, 512), (5, 1024, 8)])
+@pytest.mark.parametrize("R,K,d_out", [(48, 4096, 256), (16, 32768, 512), (5, 1024, 8),
+                                       # ragged M, K and N tiles; one partial K slice
+                                       (300, 72, 264), (130, 8, 520),
+                                       # 224 output tiles: CTAs run several, both accumulators
+                                       (1024, 128, 7168)])
 def test_oproj_matches_the_oracle(R, K, d_out):
     import torch
     from deepseek_v4_top_gb300 import dsa
