@@ -127,95 +127,8 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
 __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p) {
     grid_launch_dependents();
     grid_dependency_wait();          // the split kernel's partials are complete
-    const int r = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const float* ml_base = p.part + static_cast<size_t>(p.units) * kHeadsPad * kD;
-    const size_t u0 = static_cast<size_t>(r) * p.chunks;
-    // Up to kBatch chunks: every load (m, l and this thread's float4 of O for
-    // each chunk) is issued at once, then the maximum, then the sums in chunk
-    // order.  More chunks: a first pass over m for the maximum, then the
-    // chunks kBatch at a time.  Both give the same arithmetic.
-    constexpr int kBatch = 8;
-    float M = -INFINITY;
-    bool have = false;
-    float l = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (p.chunks <= kBatch) {
-        float mv[kBatch], lv[kBatch];
-        float4 ov[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            if (j < p.chunks) {
-                const size_t u = u0 + j;
-                mv[j] = ml_base[u * 2 * kHeadsPad + h];
-                lv[j] = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
-                ov[j] = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
-            } else {
-                mv[j] = -INFINITY;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) merge_max(M, have, mv[j]);
-        const float mu = merge_ref(M, have);
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            if (j < p.chunks) {
-                const float w = merge_weight(mv[j], mu);
-                l = fmaf(w, lv[j], l);
-                acc.x = fmaf(w, ov[j].x, acc.x);
-                acc.y = fmaf(w, ov[j].y, acc.y);
-                acc.z = fmaf(w, ov[j].z, acc.z);
-                acc.w = fmaf(w, ov[j].w, acc.w);
-            }
-        }
-        M = mu;
-    } else {
-        for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
-            float mv[kBatch];
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-                mv[j] = c0 + j < p.chunks ? ml_base[(u0 + c0 + j) * 2 * kHeadsPad + h] : -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) merge_max(M, have, mv[j]);
-        }
-        const float mu = merge_ref(M, have);
-        for (int c0 = 0; c0 < p.chunks; c0 += kBatch) {
-            float mv[kBatch], lv[kBatch];
-            float4 ov[kBatch];
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (c0 + j < p.chunks) {
-                    const size_t u = u0 + c0 + j;
-                    mv[j] = ml_base[u * 2 * kHeadsPad + h];
-                    lv[j] = ml_base[u * 2 * kHeadsPad + kHeadsPad + h];
-                    ov[j] = reinterpret_cast<const float4*>(p.part + (u * kHeadsPad + h) * kD)[tid];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (c0 + j < p.chunks) {
-                    const float w = merge_weight(mv[j], mu);
-                    l = fmaf(w, lv[j], l);
-                    acc.x = fmaf(w, ov[j].x, acc.x);
-                    acc.y = fmaf(w, ov[j].y, acc.y);
-                    acc.z = fmaf(w, ov[j].z, acc.z);
-                    acc.w = fmaf(w, ov[j].w, acc.w);
-                }
-            }
-        }
-        M = mu;
-    }
-    const float mu = M;
-    const float f = merge_factor(mu, l, p.sink[h]);
-    const float4 res = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
-    const size_t o0 = (static_cast<size_t>(r) * p.H + h) * kD;
-    if (p.out_bf16) {
-        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o0) + 2 * tid;
-        o2[0] = __floats2bfloat162_rn(res.x, res.y);
-        o2[1] = __floats2bfloat162_rn(res.z, res.w);
-    } else {
-        reinterpret_cast<float4*>(static_cast<float*>(p.out) + o0)[tid] = res;
-    }
+    merge_row_head(p.part, p.units, p.chunks, p.H, blockIdx.x, blockIdx.y, threadIdx.x, p.sink[blockIdx.y],
+                   p.out, p.out_bf16);
 }
 
 }  // namespace
