@@ -411,6 +411,52 @@ def bench_topk(args, world, rank, local):
         print(json.dumps({"metric": "top-k selection (k=%d), ms per call" % K, "workloads": out}), flush=True)
 
 
+def bench_oproj(args, world, rank, local):
+    """The output projection alone (for profiling): out [2048, 7168] fp32 =
+    attn [2048, K] bf16 . w_o [K, 7168] bf16 (K = 32768 unless --oproj-k),
+    through dsa_oproj and, for comparison, cuBLAS (torch.matmul, bf16 out),
+    each call alone with the L2 flushed before it."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    Kp, N = args.oproj_k, OPROJ_D_OUT
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xD5A0 + 18)
+    a = torch.randn((PRE_R, Kp), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((Kp, N), generator=g, device=dev) * Kp ** -0.5).to(torch.bfloat16)
+    out = torch.empty((PRE_R, N), dtype=torch.float32, device=dev)
+    ref = torch.empty((PRE_R, N), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("dsa_oproj", lambda: dsa.dsa_oproj(a, w, out, stream)),
+                     ("cublas", lambda: torch.matmul(a, w, out=ref))):
+        for _ in range(args.warmup):
+            flush.fill_(0.5)
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(max(1, args.steps))]
+        hold_gpu(stream)
+        for i, (e0, e1) in enumerate(ev):
+            flush.fill_(float(i))
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / len(ev)
+        res[name] = {"ms": ms, "tflops": 2.0 * PRE_R * Kp * N / (ms * 1e-3) / 1e12}
+    assert dsa.dsa_get_device_error() == 0
+    if rank == 0:
+        print(json.dumps({"metric": "output projection %dx%dx%d, ms per call" % (PRE_R, Kp, N),
+                          "workloads": res}), flush=True)
+
+
 def bench_ours(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
@@ -857,11 +903,14 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk", "decode_rows"), default="both",
+    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk", "decode_rows", "oproj"),
+                    default="both",
                     help="both (the benchmark step), one half of it for profiling, the top-k "
                          "selection alone, or decode with --rows-per-slot rows a slot alone")
     ap.add_argument("--rows-per-slot", type=int, default=2,
                     help="rows a slot of the decode_rows workload")
+    ap.add_argument("--oproj-k", type=int, default=H * D,
+                    help="inner size of the oproj workload (a smaller one for profiling)")
     ap.add_argument("--tp", action="store_true",
                     help="split the 64 heads over the ranks (head-sharded tensor parallelism) instead of "
                          "running independent replicas")
@@ -875,6 +924,8 @@ def main(argv=None):
         bench_topk(args, world, rank, local)
     elif args.workload == "decode_rows":
         bench_decode_rows(args, world, rank, local)
+    elif args.workload == "oproj":
+        bench_oproj(args, world, rank, local)
     elif args.tp:
         bench_tp(args, world, rank, local)
     else:
