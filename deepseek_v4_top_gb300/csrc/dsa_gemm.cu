@@ -215,12 +215,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) dsa_gemm_kernel(const __grid_
 // own 128 columns of B (32 KB a K slice instead of 48 KB), so an SM takes in
 // a third less data per MMA; the even CTA issues M = 256 MMAs that read both
 // CTAs' halves and write each CTA's 128 accumulator rows into its own TMEM.
-// Six 32 KB stages.  The stage-full barriers live in the even CTA (both
+// Seven 32 KB stages.  The stage-full barriers live in the even CTA (both
 // CTAs' TMA loads complete their bytes there), the stage-empty and
 // accumulator-full barriers in each CTA (the even CTA's commits arrive on
 // both), the accumulator-empty barriers in the even CTA (both CTAs'
 // epilogue warps arrive).
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 7;
 constexpr uint32_t kPairBBytes = 2 * kBBoxBytes;                 // 16 KB: 64 K-rows x 128 columns
 constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;      // 32 KB
 constexpr int kPairBM = 256;

@@ -76,8 +76,10 @@ def test_ties_signed_zeros_infinities_and_nans(k):
 
 
 @pytest.mark.parametrize("k", [7, 640, 2048])
-def test_specials_on_rows_split_over_a_cluster(k):
-    # ties, signed zeros, infinities and NaNs whose runs cross the CTAs of a row
+def test_specials_on_long_rows(k):
+    # rows over 4096 positions (selected in two steps: each 4096-position
+    # share, then the shares' picks): ties, signed zeros, infinities and NaNs
+    # whose runs cross the shares
     rng = np.random.default_rng(5050 + k)
     R, ld = 6, 9000
     scores = special_scores(rng, (R, ld))
@@ -86,11 +88,12 @@ def test_specials_on_rows_split_over_a_cluster(k):
     assert code == 0
 
 
-def test_all_scores_equal_and_all_nan():
-    scores = np.zeros((3, 1024), np.float32)
+@pytest.mark.parametrize("ld", [1024, 20000])
+def test_all_scores_equal_and_all_nan(ld):
+    scores = np.zeros((3, ld), np.float32)
     scores[1] = np.nan
     scores[2, ::2] = -0.0
-    code, _ = check(scores, np.array([1024, 1024, 777], np.int32), 640)
+    code, _ = check(scores, np.array([ld, ld, ld - 247], np.int32), 640)
     assert code == 0
 
 
@@ -104,9 +107,9 @@ def test_long_rows_and_row_stride():
 
 @pytest.mark.parametrize("ld", [3000, 4092, 4096, 4100, 5000, 12000, 28676])
 def test_row_strides_and_ragged_tails(ld):
-    # row strides on both sides of 4096 (one CTA a row below, a cluster of
-    # ceil(ld / 4096) CTAs a row above), candidate
-    # counts ending at every offset within a float4 and within a thread's run
+    # row strides on both sides of 4096 (one step below, two steps above),
+    # candidate counts ending at every offset within a float4 and within a
+    # thread's run
     rng = np.random.default_rng(5150 + ld)
     scores = rng.standard_normal((8, ld), dtype=np.float32)
     scores[:, 5:40] = 1.5             # ties straddling the threshold
