@@ -90,7 +90,8 @@ __device__ __forceinline__ int share_len(int n, int c) {
 }
 
 template <int kThreads, int kMode>
-__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 4 : 1) dsa_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kThreads, kThreads == 256 && kMode != kCandToIdx ? 4 : 1)
+    dsa_topk_kernel(const TopkParams p) {
     using Smem = TopkSmem<kThreads>;
     constexpr int kWarps = Smem::kWarps;
     constexpr int kB = Smem::kBinsPerThread;
@@ -144,20 +145,31 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 4 : 1) dsa_topk_ke
             continue;
         }
 
-        // 1. keys of this thread's entries
+        // 1. keys of this thread's entries (and, for the shares' picks, their
+        //    positions, loaded with them rather than one by one as picks are written)
         const int j0 = tid * kTopkPerThread;
         const int rem = n_seg - j0;  // this thread's entries: the first min(max(rem, 0), 16)
         uint32_t key[kTopkPerThread];
+        int32_t cpos[kMode == kCandToIdx ? kTopkPerThread : 1];
         if (kMode == kCandToIdx) {
             const uint4* src4 = reinterpret_cast<const uint4*>(cand_key) + j0 / 4;
+            const int4* pos4 = reinterpret_cast<const int4*>(cand_pos) + j0 / 4;
 #pragma unroll
             for (int i = 0; i < kTopkPerThread / 4; ++i) {
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (4 * i < rem) v = src4[i];
+                int4 w = make_int4(0, 0, 0, 0);
+                if (4 * i < rem) {
+                    v = src4[i];
+                    w = pos4[i];
+                }
                 key[4 * i] = 4 * i < rem ? v.x : 0u;
                 key[4 * i + 1] = 4 * i + 1 < rem ? v.y : 0u;
                 key[4 * i + 2] = 4 * i + 2 < rem ? v.z : 0u;
                 key[4 * i + 3] = 4 * i + 3 < rem ? v.w : 0u;
+                cpos[(4 * i) % (kMode == kCandToIdx ? kTopkPerThread : 1)] = w.x;
+                cpos[(4 * i + 1) % (kMode == kCandToIdx ? kTopkPerThread : 1)] = w.y;
+                cpos[(4 * i + 2) % (kMode == kCandToIdx ? kTopkPerThread : 1)] = w.z;
+                cpos[(4 * i + 3) % (kMode == kCandToIdx ? kTopkPerThread : 1)] = w.w;
             }
         } else {
             const float4* src4 =
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 4 : 1) dsa_topk_ke
                 cand_key[at0 + a] = key[i];
                 cand_pos[at0 + a] = share0 + j0 + i;
             } else {
-                out[a] = cand_pos[j0 + i];
+                out[a] = cpos[i % (kMode == kCandToIdx ? kTopkPerThread : 1)];
             }
         };
         if (need == 0u) {
