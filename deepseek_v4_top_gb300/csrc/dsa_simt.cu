@@ -3,10 +3,11 @@
 //
 // fp32 inputs need fp32 products to hold a 1e-5 relative error, which the
 // tf32 tensor-core path cannot give, so this kernel uses FFMA.  One CTA per
-// (head, row); 16-key tiles of gathered rows in shared memory; an exact
-// running maximum per tile (akol1 TensorFold PR #4, first commit message:
-// running maximum, tile sum, value sum), precise expf, the sink folded in at
-// the end (TensorFold PR #1206, "What changes").
+// (row, group of 8 heads), one warp per head: each 16-key tile of gathered
+// rows is staged in shared memory once and serves the group's 8 heads.  An
+// exact running maximum per tile (akol1 TensorFold PR #4, first commit
+// message: running maximum, tile sum, value sum), precise expf, the sink
+// folded in at the end (TensorFold PR #1206, "What changes").
 #include <math.h>
 #include <stdint.h>
 
@@ -19,8 +20,10 @@
 namespace dsa {
 namespace {
 
-constexpr int kSimtThreads = 128;
+constexpr int kSimtHeads = 8;                 // heads (warps) a CTA
+constexpr int kSimtThreads = 32 * kSimtHeads;
 constexpr int kSimtTile = 16;
+constexpr size_t kSimtSmem = (static_cast<size_t>(kSimtHeads) + kSimtTile) * kD * sizeof(float);
 
 #define DSA_R8(x) x, x, x, x, x, x, x, x
 #define DSA_R64(x) DSA_R8(DSA_R8(x))
@@ -29,78 +32,96 @@ __device__ __align__(16) uint32_t kNanRowF32[512] = {
     DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u),
     DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u), DSA_R64(0x7FC00000u)};
 
+// Warp w handles head 8 blockIdx.x + w of row blockIdx.y; lane l owns the
+// output columns l + 32 i.  A key's score is the lane's in-order FFMA sum
+// over its 16 columns, then a fixed butterfly over the lanes.
 __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams p) {
-    __shared__ __align__(16) float qs[kD];
-    __shared__ __align__(16) float kvs[kSimtTile][kD];
-    __shared__ float sc[kSimtTile];
-    __shared__ float ps[kSimtTile];
+    extern __shared__ __align__(16) float simt_smem[];
+    float* qs = simt_smem;                                // [8][512]
+    float* kvs = simt_smem + kSimtHeads * kD;             // [16][512]
 
-    const int h = blockIdx.x, r = blockIdx.y;
+    const int r = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = kSimtHeads * blockIdx.x + warp;
+    const bool live = h < p.H;
 
-    const float* qrow = p.q + (static_cast<size_t>(r) * p.H + h) * kD;
-    reinterpret_cast<float4*>(qs)[tid] = reinterpret_cast<const float4*>(qrow)[tid];
+    if (live) {
+        const float4* qrow = reinterpret_cast<const float4*>(p.q + (static_cast<size_t>(r) * p.H + h) * kD);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(qs + warp * kD)[lane + 32 * i] = qrow[lane + 32 * i];
+    }
 
     const int ns = p.n_sel[r];
     const bool bad_n = ns < 0 || ns > p.k_max;
-    if (bad_n && h == 0 && tid == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
+    if (bad_n && blockIdx.x == 0 && tid == 0) atomicOr(p.err, DSA_DEVERR_NSEL_RANGE);
     const int eff = bad_n ? 1 : ns;
     const float* cache = p.kv + (p.decode ? static_cast<size_t>(r / p.decode) * p.N * kD : 0);
     const float* nan_row = reinterpret_cast<const float*>(kNanRowF32);
 
     float m = -INFINITY, l = 0.0f;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float acc[kD / 32];
+#pragma unroll
+    for (int i = 0; i < kD / 32; ++i) acc[i] = 0.0f;
 
     for (int t0 = 0; t0 < eff; t0 += kSimtTile) {
         const int nk = min(kSimtTile, eff - t0);
-        // gather: nk rows, thread tid copies float4 number tid of each row
-        for (int j = 0; j < nk; ++j) {
+        __syncthreads();             // the previous tile's rows have been read
+        // gather: row j = e / 128 of the tile, float4 e % 128 of the row
+        for (int e = tid; e < nk * (kD / 4); e += kSimtThreads) {
+            const int j = e / (kD / 4), c4 = e - j * (kD / 4);
             const float* src = nan_row;
             if (!bad_n) {
                 const int id = p.idx[static_cast<size_t>(r) * p.k_max + t0 + j];
                 if (id >= 0 && id < p.N) {
                     src = cache + static_cast<size_t>(id) * kD;
-                } else if (h == 0 && tid == 0) {
+                } else if (blockIdx.x == 0 && c4 == 0) {
                     atomicOr(p.err, DSA_DEVERR_IDX_RANGE);
                 }
             }
-            reinterpret_cast<float4*>(kvs[j])[tid] = reinterpret_cast<const float4*>(src)[tid];
+            reinterpret_cast<float4*>(kvs + j * kD)[c4] = reinterpret_cast<const float4*>(src)[c4];
         }
         __syncthreads();
-        // scores: warp w takes keys 4w .. 4w+3; lane sums d = lane + 32 i in order
+        if (!live) continue;
+        // scores of the tile's keys for this warp's head (every lane ends with all)
+        float sc[kSimtTile];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int j = warp * 4 + jj;
+        for (int j = 0; j < kSimtTile; ++j) {
+            float part = 0.0f;
             if (j < nk) {
-                float part = 0.0f;
 #pragma unroll
-                for (int i = 0; i < kD / 32; ++i) part = fmaf(qs[lane + 32 * i], kvs[j][lane + 32 * i], part);
+                for (int i = 0; i < kD / 32; ++i)
+                    part = fmaf(qs[warp * kD + lane + 32 * i], kvs[j * kD + lane + 32 * i], part);
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if (lane == 0) sc[j] = part * p.scale;
             }
+            sc[j] = part * p.scale;
         }
-        __syncthreads();
         float tm = -INFINITY;
-        for (int j = 0; j < nk; ++j) tm = fmaxf(tm, sc[j]);
+#pragma unroll
+        for (int j = 0; j < kSimtTile; ++j)
+            if (j < nk) tm = fmaxf(tm, sc[j]);
         const float mn = (m == -INFINITY) ? tm : fmaxf(m, tm);
         const float mu_new = (mn == -INFINITY) ? 0.0f : mn;
         const float al = (m == -INFINITY) ? 1.0f : expf(m - mu_new);
-        if (tid < nk) ps[tid] = expf(sc[tid] - mu_new);
-        __syncthreads();
+        float ps[kSimtTile];
         float ls = 0.0f;
-        for (int j = 0; j < nk; ++j) ls += ps[j];
+#pragma unroll
+        for (int j = 0; j < kSimtTile; ++j) {
+            ps[j] = j < nk ? expf(sc[j] - mu_new) : 0.0f;
+            if (j < nk) ls += ps[j];
+        }
         l = l * al + ls;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int d = tid + 128 * i;
+        for (int i = 0; i < kD / 32; ++i) {
             float a = acc[i] * al;
-            for (int j = 0; j < nk; ++j) a = fmaf(ps[j], kvs[j][d], a);
+#pragma unroll
+            for (int j = 0; j < kSimtTile; ++j)
+                if (j < nk) a = fmaf(ps[j], kvs[j * kD + lane + 32 * i], a);
             acc[i] = a;
         }
         m = mn;
-        __syncthreads();
     }
+    if (!live) return;
 
     // sink fold: out = acc * e^{mu - m*} / (l e^{mu - m*} + e^{sink - m*})
     const float mu = (m == -INFINITY) ? 0.0f : m;
@@ -113,11 +134,11 @@ __global__ void __launch_bounds__(kSimtThreads) dsa_simt_kernel(const SimtParams
     if (p.out_bf16) {
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + o0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = __float2bfloat16_rn(acc[i] * f);
+        for (int i = 0; i < kD / 32; ++i) orow[lane + 32 * i] = __float2bfloat16_rn(acc[i] * f);
     } else {
         float* orow = static_cast<float*>(p.out) + o0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) orow[tid + 128 * i] = acc[i] * f;
+        for (int i = 0; i < kD / 32; ++i) orow[lane + 32 * i] = acc[i] * f;
     }
 }
 
@@ -134,8 +155,19 @@ __global__ void __launch_bounds__(128) dsa_combine_kernel(const CombineParams p)
 }  // namespace
 
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t s) {
-    dim3 grid(p.H, p.R);
-    dsa_simt_kernel<<<grid, kSimtThreads, 0, s>>>(p);
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(dsa_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSimtSmem));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid((p.H + kSimtHeads - 1) / kSimtHeads, p.R);
+    dsa_simt_kernel<<<grid, kSimtThreads, kSimtSmem, s>>>(p);
     return cudaGetLastError();
 }
 

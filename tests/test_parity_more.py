@@ -140,3 +140,12 @@ def test_decode_rows_match_across_combine_paths():
         got, code = run(sub)
         assert code == 0
         assert np.array_equal(got.view(np.uint32), full[:n].view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("H", [1, 13])
+def test_fp32_head_counts_off_the_warp_groups(mode, H):
+    # the fp32 kernel gives each CTA 8 heads (one warp each) of one row; head
+    # counts that leave a group partly empty
+    rng = np.random.default_rng(4800 + H)
+    _check(I._edge_base(rng, "f32_h%d_%s" % (H, mode), I.F32, H, 70, mode, R=3, N=600, k_extra=3))
