@@ -156,3 +156,44 @@ def test_decode_rows_host_validation(lib):
     assert call(B=1 << 20, T=1 << 12) == dsa.DSA_ERR_INVALID_ARG     # rows beyond int range
     assert call(q=0) == dsa.DSA_ERR_INVALID_ARG
     assert call(B=0, q=0, out=0) == dsa.DSA_OK
+
+
+def test_decode_cache_limit_counts_slots_not_rows(lib):
+    # 2 slots x 16384 rows a slot over 65536 positions: rows x N reaches 2^31,
+    # slots x N does not, so the call passes the host checks (on a machine
+    # without a GPU it then fails at the device, not on its arguments)
+    st = lib.dsa_sparse_attn_decode_rows(FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 1 << 14, 64, 1 << 16, 8,
+                                         dsa.DSA_BF16, None)
+    assert st != dsa.DSA_ERR_INVALID_ARG
+    st = lib.dsa_sparse_attn_decode_rows(FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 1 << 15, 1, 64, 1 << 16, 8,
+                                         dsa.DSA_BF16, None)
+    assert st == dsa.DSA_ERR_INVALID_ARG          # 32768 slots x 65536 positions
+
+
+def test_head_shard_kernels_host_validation(lib):
+    def shard(**kw):
+        a = dict(q=FAKE, sink=FAKE, ql=FAKE, sl=FAKE, R=4, H=64, world=4, rank=1, dtype=dsa.DSA_BF16)
+        a.update(kw)
+        return lib.dsa_shard_heads(a["q"], a["sink"], a["ql"], a["sl"], a["R"], a["H"], a["world"], a["rank"],
+                                   a["dtype"], None)
+    for ptr in ("q", "sink", "ql", "sl"):
+        assert shard(**{ptr: 0}) == dsa.DSA_ERR_INVALID_ARG
+    assert shard(q=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG
+    assert shard(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert shard(rank=4) == dsa.DSA_ERR_INVALID_ARG
+    assert shard(world=0) == dsa.DSA_ERR_INVALID_ARG
+    assert shard(H=300, world=2) == dsa.DSA_ERR_UNSUPPORTED   # 150 heads a rank
+    assert shard(dtype=7) == dsa.DSA_ERR_UNSUPPORTED
+    assert shard(R=0, q=0, sink=0, ql=0, sl=0) == dsa.DSA_OK
+
+    def unshard(**kw):
+        a = dict(g=FAKE, out=FAKE, R=4, H=64, world=4, dtype=dsa.DSA_F32)
+        a.update(kw)
+        return lib.dsa_unshard_heads(a["g"], a["out"], a["R"], a["H"], a["world"], a["dtype"], None)
+    assert unshard(g=0) == dsa.DSA_ERR_INVALID_ARG
+    assert unshard(out=0) == dsa.DSA_ERR_INVALID_ARG
+    assert unshard(out=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
+    assert unshard(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert unshard(world=-2) == dsa.DSA_ERR_INVALID_ARG
+    assert unshard(dtype=5) == dsa.DSA_ERR_UNSUPPORTED
+    assert unshard(R=0, g=0, out=0) == dsa.DSA_OK

@@ -209,3 +209,25 @@ def test_one_rank_step_equals_the_plain_call(lib):
     dsa.tp_sparse_attn(ql, d["kv"], d["idx"], d["n_sel"], sl, c.scale, ol, None, out2)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_one_rank_step_with_bf16_outputs(lib):
+    """The step also carries bf16 outputs (the output projection's input):
+    the same bytes as the plain call's bf16 output."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    from gpu_helpers import to_device
+    torch.cuda.set_device(0)
+    c = I.batched_decode(B=3, N=2048)
+    d = to_device(c)
+    out = torch.empty((c.R, c.H, 512), dtype=torch.bfloat16, device="cuda")
+    dsa.dsa_sparse_attn(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], c.scale, out, rows_per_slot=1)
+    ql = torch.empty_like(d["q"])
+    sl = torch.empty_like(d["sink"])
+    dsa.dsa_shard_heads(d["q"], d["sink"], ql, sl, 1, 0)
+    ol = torch.empty_like(out)
+    out2 = torch.empty_like(out)
+    dsa.tp_sparse_attn(ql, d["kv"], d["idx"], d["n_sel"], sl, c.scale, ol, None, out2, rows_per_slot=1)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
