@@ -108,3 +108,21 @@ def test_noalloc_rejects_batches_beyond_its_fixed_scratch():
     st = dsa.call_raw("dsa_sparse_attn_decode_noalloc", fake, fake, fake, fake, fake, 0.1, fake,
                       2, 64, 4096, 640, dsa.DSA_F32, 0)
     assert st == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_noalloc_after_shutdown_looks_its_array_up_again():
+    """dsa_shutdown() releases the library's device state and forgets the
+    array's looked-up address; the next call looks it up again and gives the
+    same bytes as before."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    case = I.batched_decode(B=4, N=4096)
+    d = to_device(case)
+    before = _call("dsa_sparse_attn_decode_noalloc", case, d)
+    torch.cuda.synchronize()
+    dsa.dsa_shutdown()
+    after = _call("dsa_sparse_attn_decode_noalloc", case, d)
+    again = _call("dsa_sparse_attn_decode", case, d)
+    assert np.array_equal(before.view(np.uint32), after.view(np.uint32))
+    assert np.array_equal(before.view(np.uint32), again.view(np.uint32))
+    assert dsa.dsa_get_device_error() == 0
