@@ -49,7 +49,9 @@ dsa_status device_state(DeviceState** out) {
         uint32_t* e = nullptr;
         const size_t bytes = (4 + 2 * kQueues) * sizeof(uint32_t);
         if (cudaMalloc(&e, bytes) != cudaSuccess) return DSA_ERR_CUDA;
-        if (cudaMemset(e, 0, bytes) != cudaSuccess) {
+        // zeroed on the legacy stream: wait, so that a non-blocking stream
+        // never sees the block before the memset ran
+        if (cudaMemset(e, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
             cudaFree(e);
             return DSA_ERR_CUDA;
         }
