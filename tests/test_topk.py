@@ -129,6 +129,26 @@ def test_bad_counts_set_the_error_bit_and_select_nothing():
     assert np.array_equal(idx, ref_idx) and np.array_equal(n_sel, ref_n)
 
 
+@pytest.mark.parametrize("ld", [1028, 4096])
+def test_more_rows_than_fit_at_once(ld):
+    # more rows than the GPU runs CTAs at once, with bad counts, rows whose
+    # entries are all picks, empty rows, ragged tails and specials interleaved
+    from deepseek_v4_top_gb300 import dsa
+    rng = np.random.default_rng(5300 + ld)
+    R = 1500
+    scores = rng.standard_normal((R, ld), dtype=np.float32)
+    scores[::7] = special_scores(rng, scores[::7].shape)
+    n_valid = rng.integers(1, ld + 1, R).astype(np.int32)
+    n_valid[::11] = rng.integers(0, 101, n_valid[::11].shape)   # all picks (k = 100), some empty
+    n_valid[5::13] = ld + 1 + rng.integers(0, 4, n_valid[5::13].shape)
+    n_valid[9::17] = -1
+    n_valid[-1] = ld
+    got_idx, got_n, code = gpu_topk(scores, n_valid, 100, 130)
+    ref_idx, ref_n, bad = oracle.topk(scores, n_valid, 100, 130)
+    assert np.array_equal(got_n, ref_n) and np.array_equal(got_idx, ref_idx)
+    assert bad.any() and code & dsa.DSA_DEVERR_NVALID_RANGE
+
+
 def test_repeats_are_identical():
     scores, n_valid = I.indexer_scores("prefill", rows=256)
     first = gpu_topk(scores, n_valid, 640)
