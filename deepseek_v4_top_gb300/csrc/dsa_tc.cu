@@ -506,8 +506,9 @@ __device__ bool new_reference(const TcParams& p, Misc& ms, WorkerCtx& c, uint32_
 // reference is still -inf (no finite score yet) weighs against 0 instead,
 // on a separate path that the warp takes as a whole (its lanes share their
 // heads).  Returns whether a valid score passes its reference by more than
-// 2^kTau.
-template <bool kSeen = false>
+// 2^kTau (the largest exponent against kTau: a NaN exponent passes nothing).
+// kFull: every key of the tile is valid, so no weight needs masking.
+template <bool kSeen = false, bool kFull = false>
 __device__ __forceinline__ bool tile_weights(float* x, bool valid, float sc, const float* mref, bool ninf,
                                              uint32_t* seen = nullptr) {
     bool ovf = false;
@@ -515,21 +516,25 @@ __device__ __forceinline__ bool tile_weights(float* x, bool valid, float sc, con
         // references from the sinks (all finite); bit h of *seen: this key
         // gives head h a weight of at least 2^kLowest
         uint32_t m = 0;
+        float dmax = -INFINITY;
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
             const float d = fmaf(x[h], sc, -mref[h]);
-            ovf |= d > kTau;
+            dmax = fmaxf(dmax, d);
             m |= (d >= kLowest) ? (1u << h) : 0u;
-            x[h] = valid ? ex2_approx_ftz(d) : 0.0f;
+            x[h] = (kFull || valid) ? ex2_approx_ftz(d) : 0.0f;
         }
+        ovf = dmax > kTau;
         *seen = valid ? m : 0u;
     } else if (!ninf) {
+        float dmax = -INFINITY;
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
             const float d = fmaf(x[h], sc, -mref[h]);
-            ovf |= d > kTau;
-            x[h] = valid ? ex2_approx_ftz(d) : 0.0f;
+            dmax = fmaxf(dmax, d);
+            x[h] = (kFull || valid) ? ex2_approx_ftz(d) : 0.0f;
         }
+        ovf = dmax > kTau;
     } else {
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
@@ -626,14 +631,18 @@ __device__ __forceinline__ bool softmax_tile(const TcParams& p, uint8_t* smem, M
     }
     tmem_ld32(ts, x);
     bool ovf;
+    const bool full = (t + 1) * 128 <= un.n_valid;      // the same in every thread
     if (seeded) {
         uint32_t seen;
-        ovf = tile_weights<true>(x, valid, p.scale_log2, mref, false, &seen);
+        ovf = full ? tile_weights<true, true>(x, valid, p.scale_log2, mref, false, &seen)
+                   : tile_weights<true>(x, valid, p.scale_log2, mref, false, &seen);
         seen = __reduce_or_sync(0xffffffffu, seen);
         if (c.lane == 0 && seen) atomicOr(&ms.seen[c.hf], seen);
     } else {
         // an exact first tile's references are its maxima: nothing can pass them
-        ovf = tile_weights(x, valid, p.scale_log2, mref, ninf) && t > 0;
+        ovf = (full ? tile_weights<false, true>(x, valid, p.scale_log2, mref, ninf)
+                    : tile_weights(x, valid, p.scale_log2, mref, ninf)) &&
+              t > 0;
     }
     ovf = __any_sync(0xffffffffu, ovf);
     store_p(smem, c, x);
