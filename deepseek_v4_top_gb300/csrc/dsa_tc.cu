@@ -36,8 +36,9 @@
 //     flagged first tile takes its exact maxima).  Weights are written as two bf16 terms
 //     (P = hi + lo) so the value sum keeps ~14 bits; each thread keeps its
 //     key lane's running sums, reduced over the 128 lanes once per unit.
-//   * warp 13 (one thread) loads each unit's Q by TMA once the last score
-//     MMA of the unit before has read the buffer.
+//   * warp 13 (one thread) loads each unit's Q by TMA once the workers have
+//     written P for the last tile of the unit before (its score MMAs, the
+//     last reads of Q, are done by then).
 //   * MMA warp 12 (one thread) issues tcgen05.mma:
 //       S^T[key][head]  = KV_tile (K-major, M=128) x Q^T (K-major, N=64)
 //       O^T[col][head] += V^T (MN-major, M=128 per 128 columns) x P^T
@@ -118,7 +119,8 @@ struct Misc {
     uint64_t s_full;        // MMA -> workers: scores of the tile ready
     uint64_t p_full;        // worker warps -> MMA: P written (and O^T rescaled)
     uint64_t q_full;        // Q TMA -> MMA: Q of the unit landed
-    uint64_t q_free;        // MMA -> Q warp: last score MMA of the unit done (Q may be reloaded)
+    uint64_t q_free;        // MMA -> Q warp: P of the unit's last tile written (its scores, the
+                            // last reads of Q, are done), so Q may be reloaded
     uint64_t p_ack;         // MMA -> workers: P accepted, or ms.redo set
     uint64_t red_sync;      // worker-warp sync of the tile-maxima reduction (one arrival per warp)
     uint64_t drain;         // MMA thread: everything it issued completed
@@ -372,7 +374,6 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
             tc_fence_after();
             score_mmas(tmem + kTmemS, dKv, dQ);
             umma_commit(smem_addr(&ms.s_full));
-            if (t == un.tiles - 1) umma_commit(smem_addr(&ms.q_free));
 
             // values: O^T[col][head] += V^T x (P_hi + P_lo)^T, 128 columns at a time
             if (!mbar_wait(smem_addr(&ms.p_full), ph_p, ab, p.err)) return;
@@ -395,6 +396,10 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
                 ph_p ^= 1u;
                 *reinterpret_cast<volatile int*>(&ms.redo) = 0;
             }
+            // the workers saw the unit's last score MMAs complete before they
+            // wrote P: the Q warp may load the next unit's Q (not earlier, so
+            // that its copy does not run beside this tile's softmax)
+            if (t == un.tiles - 1) mbar_arrive(smem_addr(&ms.q_free));
             mbar_arrive(smem_addr(&ms.p_ack));
             // a unit's first P.V overwrites O^T: the output warps must have read the last one
             if (t == 0 && nu > 0 && !mbar_wait(smem_addr(&ms.o_free), (nu - 1) & 1, ab, p.err)) return;
@@ -413,6 +418,7 @@ __device__ void mma_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t tm
 struct WorkerCtx {
     int wt, w, lane, qd, hf, key;   // thread, warp, lane, TMEM lane quadrant, head half, key in tile
     bool sinks;                     // every sink is finite: units start from sink references
+    float sink_mine;                // the sink reference of head 32 hf + lane (quadrant 0 publishes it)
     uint32_t lane_off;
     uint32_t ph_red, ph_ack;        // phases of red_sync and p_ack
 };
@@ -621,7 +627,7 @@ __device__ __forceinline__ bool softmax_tile(const TcParams& p, uint8_t* smem, M
             ninf = false;
             if (c.qd == 0) {
                 if (nu > 0 && !mbar_wait(smem_addr(&ms.l_free), (nu - 1) & 1, &ms.abort_flag, p.err)) return false;
-                ms.m_ref[32 * c.hf + c.lane] = sink_ref(p, 32 * c.hf + c.lane);
+                ms.m_ref[32 * c.hf + c.lane] = c.sink_mine;
             }
         } else {
             load_scores(ts, valid, p.scale_log2, x);
@@ -717,6 +723,7 @@ __device__ void worker_role(const TcParams& p, uint8_t* smem, Misc& ms, uint32_t
             // the unit starts from the sink references
 #pragma unroll
             for (int h = 0; h < 32; ++h) mref[h] = sink_ref(p, 32 * c.hf + h);
+            c.sink_mine = sink_ref(p, 32 * c.hf + c.lane);
         }
         const bool last_tile = t + 1 == un.tiles;
         const int u_next = last_tile ? unit_at(p, ms, nu + 1) : u;
@@ -781,9 +788,10 @@ __device__ void idx_role(const TcParams& p, Misc& ms, int lane) {
 }
 
 // ------------------------------------------------------------------ Q load
-// One thread of a spare warp: loads each unit's Q by tiled TMA as soon as
-// the last score MMA of the unit before has read the buffer, off the
-// workers' path.
+// One thread of a spare warp: loads each unit's Q by tiled TMA once the
+// unit before has written P for its last tile, off the workers' path (a
+// copy started as soon as the last score MMA is done ran beside that tile's
+// softmax and slowed it).
 __device__ void q_role(const TcParams& p, uint8_t* smem, Misc& ms) {
     volatile int* ab = &ms.abort_flag;
     const uint32_t sQ = smem_addr(smem + kOffQ);
