@@ -7,11 +7,12 @@
 //
 // A CTA selects over one segment of up to 16 keys a thread, held in
 // registers; thread t owns the segment's contiguous entries [16 t, 16 t + 16).
-// A row of up to 4096 positions is one segment, read as float4 (rows are
+// A row of up to 4096 positions is one segment of a 256-thread CTA, and one
+// of up to 8192 a segment of a 512-thread CTA, read as float4 (rows are
 // 16-byte aligned with a stride of a multiple of 4 scores).  A longer row is
-// selected in two steps: each 4096-position share of it selects its own top
-// k (one CTA a share, all the row's shares at once), and one CTA then selects
-// the row's top k among the shares' picks.  That is exact: a pick of the row
+// selected in two steps: each 8192-position share of it selects its own top
+// k (one 512-thread CTA a share, all the row's shares at once), and one CTA
+// then selects the row's top k among the shares' picks.  That is exact: a pick of the row
 // has fewer than k entries above it in the row, so fewer in its share.  The
 // shares' picks are stored share after share, each in position order, so the
 // second step sees them in position order too.
@@ -45,7 +46,9 @@ namespace {
 
 constexpr int kTopkBins = 2048;
 constexpr int kTopkPerThread = 16;
-constexpr int kTopkShare = 256 * kTopkPerThread;     // positions a share (and a one-step row) holds
+constexpr int kTopkShortRow = 256 * kTopkPerThread;  // rows up to this long: one 256-thread CTA
+constexpr int kTopkShare = 512 * kTopkPerThread;     // positions a share of a long row (and a one-step
+                                                     // row of 512 threads) holds
 
 // What a launch selects over and where it writes.
 enum TopkMode {
@@ -90,12 +93,14 @@ __device__ __forceinline__ int share_len(int n, int c) {
 }
 
 template <int kThreads, int kMode>
-__global__ void __launch_bounds__(kThreads, kThreads == 256 && kMode != kCandToIdx ? 4 : 1)
+__global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads == 256 ? 4 : 2))
     dsa_topk_kernel(const TopkParams p) {
     using Smem = TopkSmem<kThreads>;
     constexpr int kWarps = Smem::kWarps;
     constexpr int kB = Smem::kBinsPerThread;
     static_assert(kB >= 2 && kThreads * kB == kTopkBins, "bin ownership");
+    static_assert(kMode != kSharesToCand || kThreads * kTopkPerThread == kTopkShare, "a share a CTA");
+    static_assert(kTopkMaxLd / kTopkShare * kTopkMaxK <= 512 * kTopkPerThread, "a long row's picks fit 512 threads");
     __shared__ Smem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_launch_dependents();
@@ -339,17 +344,18 @@ int topk_shares(int ld) { return ld <= kTopkShare ? 1 : (ld + kTopkShare - 1) / 
 cudaError_t launch_topk(const TopkParams& p, int grid, cudaStream_t s) {
     if (p.ld % 4 != 0 || reinterpret_cast<uintptr_t>(p.scores) % 16 != 0 || p.ld > kTopkMaxLd)
         return cudaErrorInvalidValue;
-    if (p.shares == 1) return launch_mode<256, kRowsToIdx>(p, grid, s);
+    if (p.shares == 1)
+        return p.ld <= kTopkShortRow ? launch_mode<256, kRowsToIdx>(p, grid, s) : launch_mode<512, kRowsToIdx>(p, grid, s);
     // long rows: the shares' selections, then one over their picks
-    if (p.cand_ld % 4 != 0 || p.cand_ld < p.shares * p.k || p.shares * p.k > 1024 * kTopkPerThread)
+    if (p.cand_ld % 4 != 0 || p.cand_ld < p.shares * p.k || p.shares * p.k > 512 * kTopkPerThread)
         return cudaErrorInvalidValue;
     const long long share_grid = static_cast<long long>(grid) * p.shares;
-    cudaError_t e = launch_mode<256, kSharesToCand>(p, static_cast<int>(share_grid), s);
+    cudaError_t e = launch_mode<512, kSharesToCand>(p, static_cast<int>(share_grid), s);
     if (e != cudaSuccess) return e;
     const int cap = p.shares * p.k;
+    // (at most 32768 / 8192 = 4 shares of 2048 picks: 8192 candidates)
     if (cap <= 256 * kTopkPerThread) return launch_mode<256, kCandToIdx>(p, grid, s);
-    if (cap <= 512 * kTopkPerThread) return launch_mode<512, kCandToIdx>(p, grid, s);
-    return launch_mode<1024, kCandToIdx>(p, grid, s);
+    return launch_mode<512, kCandToIdx>(p, grid, s);
 }
 
 }  // namespace dsa

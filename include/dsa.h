@@ -267,7 +267,7 @@ DSA_API dsa_status dsa_sparse_attn_decode_noalloc(const void* q, const void* kv_
  * no input before the work queued before it on the stream has completed.
  * DSA_ERR_INVALID_ARG for a null pointer, a misaligned scores, or bad
  * sizes; DSA_ERR_UNSUPPORTED for k > 2048 or ld > 32768.
- * Rows with ld > 4096 are selected in two steps (each 4096-position share
+ * Rows with ld > 8192 are selected in two steps (each 8192-position share
  * of a row, then the shares' picks) through a per-device scratch of up to
  * 256 MB, allocated on first use (a larger call processes its rows in turn)
  * and released by dsa_shutdown(); such calls whose work overlaps on the GPU

@@ -77,13 +77,13 @@ def test_ties_signed_zeros_infinities_and_nans(k):
 
 @pytest.mark.parametrize("k", [7, 640, 2048])
 def test_specials_on_long_rows(k):
-    # rows over 4096 positions (selected in two steps: each 4096-position
+    # rows over 8192 positions (selected in two steps: each 8192-position
     # share, then the shares' picks): ties, signed zeros, infinities and NaNs
     # whose runs cross the shares
     rng = np.random.default_rng(5050 + k)
     R, ld = 6, 9000
     scores = special_scores(rng, (R, ld))
-    n_valid = np.array([k - 1, k + 1, 4096, 4097, 8999, 9000], np.int32)
+    n_valid = np.array([k - 1, k + 1, 8192, 8193, 8999, 9000], np.int32)
     code, _ = check(scores, n_valid, k, k + 5)
     assert code == 0
 
@@ -105,9 +105,10 @@ def test_long_rows_and_row_stride():
     assert code == 0
 
 
-@pytest.mark.parametrize("ld", [3000, 4092, 4096, 4100, 5000, 12000, 28676])
+@pytest.mark.parametrize("ld", [3000, 4092, 4096, 4100, 5000, 8188, 8192, 8196, 12000, 28676])
 def test_row_strides_and_ragged_tails(ld):
-    # row strides on both sides of 4096 (one step below, two steps above),
+    # row strides on both sides of 4096 (one 256-thread CTA below, one of
+    # 512 threads above) and of 8192 (one step below, two steps above),
     # candidate counts ending at every offset within a float4 and within a
     # thread's run
     rng = np.random.default_rng(5150 + ld)
