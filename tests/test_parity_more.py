@@ -5,7 +5,9 @@
 - decode rows longer than 1024 keys (16 key chunks a row);
 - prefill rows whose unit count is not a multiple of the SM count;
 - the same calls captured into a CUDA graph, and issued on a side stream,
-  must give the same bits as direct calls on the current stream.
+  must give the same bits as direct calls on the current stream;
+- index entries past n_sel holding arbitrary values (extremes included)
+  change no output bit and raise no error.
 
 Tolerances as in test_parity.py: bf16 |g-o| <= 3e-3 * max|o| over the
 (row, head), nonfinite classes exact.
@@ -149,3 +151,38 @@ def test_fp32_head_counts_off_the_warp_groups(mode, H):
     # counts that leave a group partly empty
     rng = np.random.default_rng(4800 + H)
     _check(I._edge_base(rng, "f32_h%d_%s" % (H, mode), I.F32, H, 70, mode, R=3, N=600, k_extra=3))
+
+
+def _garbage_tail(case, seed):
+    """The same case with every idx entry past n_sel[r] replaced by arbitrary
+    int32 values, the extremes included (the header lets those entries hold
+    anything)."""
+    import copy
+    c = copy.copy(case)
+    c.idx = case.idx.copy()
+    rng = np.random.default_rng(seed)
+    for r in range(c.R):
+        tail = c.idx[r, max(int(c.n_sel[r]), 0):]
+        tail[:] = rng.integers(-2**31, 2**31, tail.shape, dtype=np.int64).astype(np.int32)
+        if tail.size >= 2:
+            tail[0], tail[-1] = np.iinfo(np.int32).max, np.iinfo(np.int32).min
+    return c
+
+
+@pytest.mark.parametrize("which", ["decode", "prefill", "decode_rows", "fp32_decode"])
+def test_unused_index_entries_may_hold_anything(which):
+    rng = np.random.default_rng(77)
+    if which == "decode":
+        case = I._edge_base(rng, "tail_decode", I.BF16, 64, 500, "decode", R=6, N=3000, k_extra=140)
+    elif which == "prefill":
+        case = I._edge_base(rng, "tail_prefill", I.BF16, 64, 300, "prefill", R=200, N=2000, k_extra=40)
+    elif which == "decode_rows":
+        case = I.multi_row_decode(B=3, T=2, N=2048, k=300)
+        case.n_sel[1::2] = case.n_sel[1::2] // 2          # half-used rows leave long tails
+    else:
+        case = I._edge_base(rng, "tail_fp32", I.F32, 16, 200, "decode", R=3, N=1000, k_extra=60)
+    want, code = run(case)
+    assert code == 0
+    got, code = run(_garbage_tail(case, 78))
+    assert code == 0, "device error word %#x" % code
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
