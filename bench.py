@@ -461,12 +461,15 @@ def bench_ours(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
     import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    __graft_entry__.build()
+    # one process a node builds (the others would write the same files), the rest wait for it
+    if local == 0:
+        __graft_entry__.build()
+    barrier(world)
     dsa.load()
     do_dec = args.workload in ("both", "decode")
     do_pre = args.workload in ("both", "prefill")
@@ -810,12 +813,15 @@ def bench_tp(args, world, rank, local):
     import torch
     from deepseek_v4_top_gb300 import dsa
     import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    __graft_entry__.build()
+    # one process a node builds (the others would write the same files), the rest wait for it
+    if local == 0:
+        __graft_entry__.build()
+    barrier(world)
     dsa.load()
     plan = dsa.dsa_head_shard(H, world, rank)
     hpr = plan.heads_per_rank
