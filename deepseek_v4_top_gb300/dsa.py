@@ -111,6 +111,17 @@ def call_raw(name: str, q: int, kv: int, idx: int, n_sel: int, sink: int, scale:
 
 
 # ------------------------------------------------------------ torch tensors
+def _same_device(*pairs):
+    """Every tensor must be on the current CUDA device: the library launches
+    there, and another device's addresses are not valid in its kernels."""
+    import torch
+    cur = torch.cuda.current_device()
+    for name, t in pairs:
+        if t.device.index != cur:
+            raise ValueError("%s is on cuda:%s, but the calls run on the current device cuda:%d "
+                             "(torch.cuda.set_device)" % (name, t.device.index, cur))
+
+
 def _dtype_code(t):
     import torch
     if t.dtype == torch.float32:
@@ -130,6 +141,7 @@ def _check(q, kv, idx, n_sel, sink, out, decode, rows_per_slot=1, out_dtype=None
             raise ValueError("%s must be a CUDA tensor" % name)
         if not t.is_contiguous():
             raise ValueError("%s must be contiguous" % name)
+    _same_device(("q", q), ("kv_cache", kv), ("idx", idx), ("n_sel", n_sel), ("sink", sink), ("out", out))
     if kv.dtype != q.dtype:
         raise TypeError("q and kv_cache must have the same dtype")
     if idx.dtype != torch.int32 or n_sel.dtype != torch.int32:
@@ -160,6 +172,10 @@ def _stream_handle(stream):
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
+    if hasattr(stream, "device") and getattr(stream.device, "index", None) is not None:
+        if stream.device.index != torch.cuda.current_device():
+            raise ValueError("the stream belongs to cuda:%d, but the calls run on the current device cuda:%d"
+                             % (stream.device.index, torch.cuda.current_device()))
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -227,6 +243,7 @@ def _check_oproj(attn, w_o, out):
     for name, t in (("attn", attn), ("w_o", w_o), ("out", out)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _same_device(("attn", attn), ("w_o", w_o), ("out", out))
     if attn.dtype != torch.bfloat16 or w_o.dtype != torch.bfloat16 or out.dtype != torch.float32:
         raise TypeError("attn and w_o must be bfloat16, out float32")
     if w_o.dim() != 2 or out.dim() != 2:
@@ -276,6 +293,7 @@ def dsa_topk_select(scores, n_valid, k, idx, n_sel, stream=None):
     for name, t in (("scores", scores), ("n_valid", n_valid), ("idx", idx), ("n_sel", n_sel)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _same_device(("scores", scores), ("n_valid", n_valid), ("idx", idx), ("n_sel", n_sel))
     if scores.dtype != torch.float32 or scores.dim() != 2:
         raise TypeError("scores must be a float32 [rows, ld] tensor")
     if n_valid.dtype != torch.int32 or idx.dtype != torch.int32 or n_sel.dtype != torch.int32:
@@ -307,6 +325,7 @@ def dsa_shard_heads(q, sink, q_local, sink_local, world: int, rank: int, stream=
     for name, t in (("q", q), ("sink", sink), ("q_local", q_local), ("sink_local", sink_local)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _same_device(("q", q), ("sink", sink), ("q_local", q_local), ("sink_local", sink_local))
     if q.dim() != 3 or q.shape[2] != 512 or q_local.dtype != q.dtype:
         raise ValueError("q [rows, heads, 512] and q_local of the same dtype expected")
     R, H = q.shape[0], q.shape[1]
@@ -329,6 +348,7 @@ def dsa_unshard_heads(gathered, out, world: int, stream=None):
     for name, t in (("gathered", gathered), ("out", out)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    _same_device(("gathered", gathered), ("out", out))
     if out.dim() != 3 or out.shape[2] != 512 or gathered.dtype != out.dtype:
         raise ValueError("out [rows, heads, 512] and gathered of the same dtype expected")
     R, H = out.shape[0], out.shape[1]

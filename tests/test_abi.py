@@ -197,3 +197,25 @@ def test_head_shard_kernels_host_validation(lib):
     assert unshard(world=-2) == dsa.DSA_ERR_INVALID_ARG
     assert unshard(dtype=5) == dsa.DSA_ERR_UNSUPPORTED
     assert unshard(R=0, g=0, out=0) == dsa.DSA_OK
+
+
+def test_binding_refuses_tensors_and_streams_of_another_device(monkeypatch):
+    """The library launches on the current device; the binding refuses a
+    tensor or a stream that lives on another one (its addresses would not be
+    valid there) before anything reaches the C ABI."""
+    import types
+
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    here = types.SimpleNamespace(device=types.SimpleNamespace(index=0))
+    there = types.SimpleNamespace(device=types.SimpleNamespace(index=1))
+    dsa._same_device(("a", here), ("b", here))
+    with pytest.raises(ValueError, match="cuda:1"):
+        dsa._same_device(("a", here), ("b", there))
+    stream = types.SimpleNamespace(device=types.SimpleNamespace(index=1), cuda_stream=1234)
+    with pytest.raises(ValueError, match="stream"):
+        dsa._stream_handle(stream)
+    ok = types.SimpleNamespace(device=types.SimpleNamespace(index=0), cuda_stream=1234)
+    assert dsa._stream_handle(ok) == 1234
+    assert dsa._stream_handle(5678) == 5678
