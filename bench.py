@@ -61,6 +61,14 @@ def dist_env():
     return world, rank, local
 
 
+def compulsory_bytes(rows: int, kv_bytes: int) -> int:
+    """Bytes a call must move to or from HBM at least: q (bf16) and idx in,
+    out (fp32) back, and the KV rows it reads (decode: the gathered rows,
+    each slot's cache being far larger than L2; prefill: the whole 4 MiB
+    cache, which then stays in L2)."""
+    return rows * H * D * 2 + rows * K * 4 + rows * H * D * 4 + kv_bytes
+
+
 def reduce_max(value: float, world: int) -> float:
     """Maximum of a per-rank float over the process group (identity when alone)."""
     if world == 1:
@@ -661,7 +669,9 @@ def bench_ours(args, world, rank, local):
             "ms": dec_avg, "ms_median": reduce_max(statistics.median(dec_ms), world),
             "row_heads_per_s": DEC_B * H / (dec_avg * 1e-3),
             "gathered_kv_gbs": g / (dec_avg * 1e-3) / 1e9,
-            "gathered_frac_hbm": g / (dec_avg * 1e-3) / 1e9 / pk["hbm_gbs"], "launches": 2}
+            "gathered_frac_hbm": g / (dec_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "compulsory_bytes": compulsory_bytes(DEC_B, g),
+            "compulsory_gbs": compulsory_bytes(DEC_B, g) / (dec_avg * 1e-3) / 1e9, "launches": 2}
         workloads["decode_b8_sustained"] = {
             "ms": dec_sus_ms, "row_heads_per_s": DEC_B * H / (dec_sus_ms * 1e-3),
             "gathered_kv_gbs": g / (dec_sus_ms * 1e-3) / 1e9,
@@ -721,6 +731,8 @@ def bench_ours(args, world, rank, local):
             "row_heads_per_s": PRE_R * H / (pre_avg * 1e-3),
             "gathered_kv_gbs": g / (pre_avg * 1e-3) / 1e9,
             "gathered_frac_hbm": g / (pre_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "compulsory_bytes": compulsory_bytes(PRE_R, PRE_N * D * 2),
+            "compulsory_gbs": compulsory_bytes(PRE_R, PRE_N * D * 2) / (pre_avg * 1e-3) / 1e9,
             "tflops": pre_tflops, "launches": 1}
         a = g / (pre_avg * 1e-3) / 1e9
         roofline = {
