@@ -369,6 +369,33 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
     return sum(ms) / reps, c.R
 
 
+def single_decode_timing(dsa, dev, flush, reps=20):
+    """Median and mean milliseconds of one single-row decode call (64 heads,
+    a 4096-position cache, 640 sorted keys), the L2 flushed before each: the
+    latency case."""
+    import torch
+    c = I.single_decode()
+    t = lambda a, bf: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+                       if bf else torch.from_numpy(a).to(dev))
+    q, kv, idx, n_sel, sink = t(c.q, True), t(c.kv, True), t(c.idx, False), t(c.n_sel, False), t(c.sink, False)
+    out = torch.empty((1, H, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, c.scale, out, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    hold_gpu(stream)
+    for i in range(reps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, c.scale, out, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    assert dsa.dsa_get_device_error() == 0
+    return statistics.median(ms), sum(ms) / reps
+
+
 def bench_decode_rows(args, world, rank, local):
     """Decode with T = --rows-per-slot rows a slot alone (for profiling): one
     JSON line with its time and the KV bytes it selects, in total and as
@@ -689,6 +716,16 @@ def bench_ours(args, world, rank, local):
             "gathered_frac_hbm": g / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "how": "dsa_sparse_attn_decode_rows, 8 slots x 2 rows (N=32768 per slot), one call a time, "
                    "L2 flushed before each"}
+        # one decode row alone: the latency case (not part of the step)
+        med, mean = single_decode_timing(dsa, dev, flush)
+        med, mean = reduce_max(med, world), reduce_max(mean, world)
+        g = K * D * 2
+        workloads["decode_b1"] = {
+            "ms": mean, "ms_median": med, "row_heads_per_s": H / (mean * 1e-3),
+            "gathered_kv_gbs": g / (mean * 1e-3) / 1e9,
+            "gathered_frac_hbm": g / (mean * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "how": "dsa_sparse_attn_decode, 1 row, 64 heads, N=4096, 640 sorted keys, one call a time, "
+                   "L2 flushed before each (split kernel + combine)"}
         # the indexer's top-k selection, timed on its own (not part of the step)
         for mode, key in (("prefill", "topk_prefill_2048"), ("decode", "topk_decode_b8")):
             t_ms, rows, nbytes = topk_timing(dsa, dev, flush, mode)
