@@ -836,7 +836,9 @@ def bench_ours(args, world, rank, local):
         "wall_s_timed_region": t_wall3 - t_wall2,
         "wall_s_one_stream_loop": t_wall1 - t_wall0,
     }
-    if rank == 0 and not args.no_cpu_baseline and do_dec and do_pre:
+    # the oracle's rate on the host cores: one GPU only, so that no rank waits
+    # on it (at N > 1 each rank's host would share its cores with the others)
+    if world == 1 and not args.no_cpu_baseline and do_dec and do_pre:
         cb = oracle_sample(pre, dec, args.cpu_seconds)
         # cores: the threads the timed oracle ran on; the host's own core
         # counts beside it
