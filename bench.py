@@ -268,7 +268,7 @@ def hold_gpu(stream, ms=2.0):
         torch.cuda._sleep(int(ms * 2.0e6))      # cycles at about 2 GHz
 
 
-def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
+def topk_timing(dsa, dev, flush, mode, k=K, reps=32):
     """Mean milliseconds of one top-k selection call over the indexer-score
     rows of `mode` (prefill: 2048 causal rows of a 4096 cache; decode: 8
     rows of 32768), the L2 flushed before each call; and the bytes of
@@ -297,7 +297,7 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=20):
     return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
 
 
-def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
+def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=32):
     """The prefill rows' attention with a bf16 output, then their output
     projection (out [2048, d_out] fp32 = attn [2048, 64*512] bf16 . w_o) by
     the library's GEMM, and, for comparison, the same product by cuBLAS
@@ -343,7 +343,7 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=20):
     return res[0], res[1], res[2]
 
 
-def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
+def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=32):
     """Mean milliseconds of one decode call with T query rows a slot (B slots
     of a 32768-position cache, k=640), the L2 flushed before each call."""
     import torch
@@ -369,7 +369,7 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=20):
     return sum(ms) / reps, c.R
 
 
-def single_decode_timing(dsa, dev, flush, reps=20):
+def single_decode_timing(dsa, dev, flush, reps=32):
     """Median and mean milliseconds of one single-row decode call (64 heads,
     a 4096-position cache, 640 sorted keys), the L2 flushed before each: the
     latency case."""
