@@ -259,7 +259,7 @@ def decode_sustained(dsa, d, case, dev):
     return e0.elapsed_time(e1) / (reps * SUS_CALLS)
 
 
-def hold_gpu(stream, ms=2.0):
+def hold_gpu(stream, ms=4.0):
     """Keep the stream busy for about `ms` milliseconds, so that the host has
     enqueued the timed calls that follow before the GPU reaches them: the
     events then time the calls, not the host's launch latency."""
