@@ -2,8 +2,10 @@
 
 One step = one batched decode call (8 slots x 32768-position caches) and one
 prefill call (2048 rows at positions 2048..4095 of a 4096-position cache), both
-with 64 heads, 512-wide latent rows, k = 640 selected keys, bf16 inputs.
-Metric: row*heads per second (whole job), plus gathered-KV GB/s per workload.
+with 64 heads, 512-wide latent rows, k = 640 selected keys, bf16 inputs; the
+two independent calls are issued on two streams at once.  Metric: row*heads
+per second (whole job), plus each call's own time and gathered-KV GB/s, timed
+one call after the other on one stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
