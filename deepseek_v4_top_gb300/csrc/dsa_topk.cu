@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
     constexpr int kB = Smem::kBinsPerThread;
     static_assert(kB >= 2 && kThreads * kB == kTopkBins, "bin ownership");
     static_assert(kMode != kSharesToCand || kThreads * kTopkPerThread == kTopkShare, "a share a CTA");
+    // rows of up to 4096 (four CTAs an SM): a thread wholly past its row's
+    // candidates holds only padding and skips the counting and compaction
+    constexpr bool kSkipPadding = kMode == kRowsToIdx && kThreads == 256;
     static_assert(kTopkMaxLd / kTopkShare * kTopkMaxK <= 512 * kTopkPerThread, "a long row's picks fit 512 threads");
     __shared__ Smem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -213,10 +216,12 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
             const int shift = digit_shift(pass), nb = digit_bins(pass);
             const int hi = shift + (pass == 2 ? 10 : 11);      // bits fixed before this pass: [hi, 32)
             const uint32_t prefix = sm.prefix;
+            if (!kSkipPadding || rem > 0) {
 #pragma unroll
-            for (int i = 0; i < kTopkPerThread; ++i) {
-                if (pass == 0 || (key[i] >> hi) == (prefix >> hi))
-                    atomicAdd(&sm.hist[bin_slot<kB>((key[i] >> shift) & static_cast<uint32_t>(nb - 1))], 1u);
+                for (int i = 0; i < kTopkPerThread; ++i) {
+                    if (pass == 0 || (key[i] >> hi) == (prefix >> hi))
+                        atomicAdd(&sm.hist[bin_slot<kB>((key[i] >> shift) & static_cast<uint32_t>(nb - 1))], 1u);
+                }
             }
             __syncthreads();
             // thread t: bins nb-1-t*B-b, b = 0 .. B-1, counted from the top
@@ -270,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
 
         // 3. this thread's keys above thr and equal to thr, packed; block scan
         uint32_t packed = 0u;
-        if (need == 0u) {
+        if (kSkipPadding && rem <= 0) {
+            // only padding: no picks
+        } else if (need == 0u) {
 #pragma unroll
             for (int i = 0; i < kTopkPerThread; ++i) packed += key[i] > thr ? 0x10000u : 0u;
         } else {
@@ -301,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
                 out[a] = cpos[i % (kMode == kCandToIdx ? kTopkPerThread : 1)];
             }
         };
-        if (need == 0u) {
+        if (kSkipPadding && rem <= 0) {
+            // only padding: no picks
+        } else if (need == 0u) {
 #pragma unroll
             for (int i = 0; i < kTopkPerThread; ++i) {
                 if (key[i] > thr) put(i, at++);
