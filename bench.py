@@ -615,15 +615,24 @@ def bench_ours(args, world, rank, local):
         pinned.append(t)
         return t
 
+    # Two sets of device inputs and outputs (and of host outputs), used by
+    # alternate steps, so that a step's copies can overlap the step before it
+    # (a serving loop double-buffers the same way); the KV caches and sinks
+    # stay resident.
     e2e_io = []
     if do_dec:
         e2e_io.append((d_dec, pin(dec.q.view(np.int16)), pin(dec.idx), pin(dec.n_sel),
-                       torch.empty(o_dec.shape, dtype=torch.float32).pin_memory(), o_dec, call_dec))
+                       [torch.empty(o_dec.shape, dtype=torch.float32).pin_memory() for _ in range(2)],
+                       [o_dec, torch.empty_like(o_dec)], False))
     if do_pre:
         e2e_io.append((d_pre, pin(pre.q.view(np.int16)), pin(pre.idx), pin(pre.n_sel),
-                       torch.empty(o_pre.shape, dtype=torch.float32).pin_memory(), o_pre, call_pre))
+                       [torch.empty(o_pre.shape, dtype=torch.float32).pin_memory() for _ in range(2)],
+                       [o_pre, torch.empty_like(o_pre)], True))
     h2d = sum(t.numel() * t.element_size() for t in pinned)
-    d2h = sum(io[4].numel() * 4 for io in e2e_io)
+    d2h = sum(io[4][0].numel() * 4 for io in e2e_io)
+    dev_in = [[(d["q"], d["idx"], d["n_sel"]) for d, *_ in e2e_io],
+              [(torch.empty_like(d["q"]), torch.empty_like(d["idx"]), torch.empty_like(d["n_sel"]))
+               for d, *_ in e2e_io]]
 
     # The step runs as a user with host-resident tensors would run it: prefill
     # rows in E2E_CHUNKS chunks over three streams (copy in, compute, copy out),
@@ -633,50 +642,66 @@ def bench_ours(args, world, rank, local):
     s_in = torch.cuda.Stream(device=dev)
     s_comp = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
+    comp_done, out_done = {}, {}
 
-    def e2e_step(start_ev):
+    def e2e_step(i, start_ev):
+        """Step i on buffer set i % 2; returns the event of its last copy out."""
+        k = i % 2
         for st in (s_in, s_comp, s_out):
             st.wait_event(start_ev)
-        done = []
-        for d, hq, hidx, hns, hout, dout, call in e2e_io:
+        # the set's inputs were last read by step i - 2's kernels, its outputs
+        # last copied out by step i - 2
+        if i - 2 in comp_done:
+            s_in.wait_event(comp_done.pop(i - 2))
+        if i - 2 in out_done:
+            s_comp.wait_event(out_done.pop(i - 2))
+        for j, (d, hq, hidx, hns, houts, douts, is_pre) in enumerate(e2e_io):
+            q, idx, n_sel = dev_in[k][j]
+            hout, dout = houts[k], douts[k]
             rows = hq.shape[0]
-            is_pre = rows == PRE_R
             chunks = E2E_CHUNKS if is_pre else 1
             bounds = [rows * c // chunks for c in range(chunks + 1)]
             for c in range(chunks):
                 a, b = bounds[c], bounds[c + 1]
                 with torch.cuda.stream(s_in):
-                    d["q"][a:b].view(torch.int16).copy_(hq[a:b], non_blocking=True)
-                    d["idx"][a:b].copy_(hidx[a:b], non_blocking=True)
-                    d["n_sel"][a:b].copy_(hns[a:b], non_blocking=True)
+                    q[a:b].view(torch.int16).copy_(hq[a:b], non_blocking=True)
+                    idx[a:b].copy_(hidx[a:b], non_blocking=True)
+                    n_sel[a:b].copy_(hns[a:b], non_blocking=True)
                     ev_in = torch.cuda.Event()
                     ev_in.record(s_in)
                 s_comp.wait_event(ev_in)
                 fn = dsa.dsa_sparse_attn_prefill if is_pre else dsa.dsa_sparse_attn_decode
-                fn(d["q"][a:b], d["kv"], d["idx"][a:b], d["n_sel"][a:b], d["sink"],
+                fn(q[a:b], d["kv"], idx[a:b], n_sel[a:b], d["sink"],
                    pre.scale if is_pre else dec.scale, dout[a:b], s_comp)
                 ev_c = torch.cuda.Event()
                 ev_c.record(s_comp)
                 s_out.wait_event(ev_c)
                 with torch.cuda.stream(s_out):
                     hout[a:b].copy_(dout[a:b], non_blocking=True)
+        ev_comp = torch.cuda.Event()
+        ev_comp.record(s_comp)
+        comp_done[i] = ev_comp
         ev_done = torch.cuda.Event()
         ev_done.record(s_out)
+        out_done[i] = ev_done
         return ev_done
 
     e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
+    for i in range(2):
         ev0 = torch.cuda.Event()
         ev0.record(stream)
-        stream.wait_event(e2e_step(ev0))
+        stream.wait_event(e2e_step(i, ev0))
     torch.cuda.synchronize()
+    comp_done.clear()
+    out_done.clear()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    last = e0
-    for _ in range(e2e_steps):
-        last = e2e_step(last)
+    last = None
+    for i in range(e2e_steps):
+        last = e2e_step(i, e0)
+    # every step's copies out are done (each stream runs in order)
     stream.wait_event(last)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -831,8 +856,9 @@ def bench_ours(args, world, rank, local):
             "d2h_bytes_per_step": d2h,
             "note": "q, idx, n_sel copied in from pinned host memory and out copied back every "
                     "step; prefill in %d row chunks over three streams (copy in, compute, copy "
-                    "out) so that both copy directions overlap the kernels; KV caches and sinks "
-                    "stay resident" % E2E_CHUNKS,
+                    "out) so that both copy directions overlap the kernels; alternate steps use two "
+                    "sets of device buffers, so a step's copies also overlap the step before it; KV "
+                    "caches and sinks stay resident" % E2E_CHUNKS,
         },
         "clocks": clocks.summary(t_wall0, t_clock1),
         "wall_s_timed_region": t_wall3 - t_wall2,
