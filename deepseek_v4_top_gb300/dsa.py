@@ -384,6 +384,51 @@ def tp_sparse_attn(q_local, kv_cache, idx, n_sel, sink_local, scale, out_local, 
         return dsa_unshard_heads(src, out, world)
 
 
+def tp_oproj_weights(w_o, H: int, world: int, rank: int):
+    """The rank's rows of the output projection w_o [H*512, d_out] (bf16) for
+    tp_sparse_attn_oproj: its heads' 512-row blocks, then zero blocks for its
+    padding heads, whose attention outputs (q = 0, sink = 0) must not reach
+    the projection.  One-time weight preparation: a view of w_o when the rank
+    has no padding heads, else a padded copy."""
+    import torch
+    if not isinstance(w_o, torch.Tensor) or w_o.dim() != 2 or w_o.shape[0] != H * 512:
+        raise ValueError("w_o must be a [heads * 512, d_out] tensor")
+    plan = dsa_head_shard(H, world, rank)
+    lo, n = plan.first_head * 512, plan.real_heads * 512
+    if plan.real_heads == plan.heads_per_rank:
+        return w_o[lo:lo + n]
+    local = torch.zeros((plan.heads_per_rank * 512, w_o.shape[1]), dtype=w_o.dtype, device=w_o.device)
+    local[:n].copy_(w_o[lo:lo + n])
+    return local
+
+
+def tp_sparse_attn_oproj(q_local, kv_cache, idx, n_sel, sink_local, scale, w_o_local, attn_local, out,
+                         group=None, rows_per_slot=0, stream=None):
+    """One rank's step of head-sharded attention followed by the output
+    projection, row-parallel, all on one stream (torch's current one unless
+    `stream` is given): the attention over the rank's heads into attn_local
+    [R,hpr,512] (bf16), the rank's share of the projection out [R,d_out] fp32
+    = attn_local . w_o_local (w_o_local from tp_oproj_weights), then a sum
+    of every rank's share over `group` (torch.distributed all-reduce; NCCL on
+    GPUs), so that every rank holds the whole projection.  Against
+    tp_sparse_attn followed by the projection, the ranks exchange the
+    projected rows (R x d_out fp32) instead of the attention outputs
+    (R x H x 512 bf16).  The shares are summed in the collective's order, so
+    the result differs from the one-GPU projection by fp32 rounding."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
+    if attn_local.dtype != torch.bfloat16:
+        raise TypeError("attn_local must be bfloat16 (the projection's A operand)")
+    with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+        dsa_sparse_attn(q_local, kv_cache, idx, n_sel, sink_local, scale, attn_local,
+                        rows_per_slot=rows_per_slot)
+        dsa_oproj(attn_local.view(attn_local.shape[0], -1), w_o_local, out)
+        if world > 1:
+            dist.all_reduce(out, op=dist.ReduceOp.SUM, group=group)
+        return out
+
+
 def dsa_selftest_wait_limit(stream=None) -> None:
     """Queue the bounded-wait self-test (sets DSA_DEVERR_TIMEOUT after ~2 s)."""
     st = load().dsa_selftest_wait_limit(_stream_handle(stream))

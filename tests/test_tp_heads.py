@@ -231,3 +231,134 @@ def test_one_rank_step_with_bf16_outputs(lib):
     dsa.tp_sparse_attn(ql, d["kv"], d["idx"], d["n_sel"], sl, c.scale, ol, None, out2, rows_per_slot=1)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+# ------------------------------------------ row-parallel output projection
+def _w_o(H, d_out, seed):
+    rng = np.random.default_rng(seed)
+    return I.f32_to_bf16_bits((rng.standard_normal((H * 512, d_out)) / np.sqrt(H * 512)).astype(np.float32))
+
+
+def _bf16_round_f64(o):
+    """The attention's fp64 result as the bf16 the GPU hands the projection
+    (fp32, then round to nearest even), as bf16 bit patterns."""
+    return I.f32_to_bf16_bits(o.astype(np.float32))
+
+
+def _oproj_worker(rank, world, port, H, d_out, q):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch
+    import torch.distributed as dist
+    import oracle
+    from deepseek_v4_top_gb300 import dsa
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    c = _case(H)
+    plan = dsa.dsa_head_shard(H, world, rank)
+    local, _ = oracle.attn(_shard_case(c, plan), threads=1)            # [R, hpr, 512], padding heads too
+    w = torch.from_numpy(_w_o(H, d_out, 33).view(np.int16))
+    w_local = dsa.tp_oproj_weights(w, H, world, rank).numpy().view(np.uint16)
+    a = _bf16_round_f64(local).reshape(c.R, -1)
+    part, _ = oracle.oproj(a, np.ascontiguousarray(w_local))          # the rank's share, fp64
+    t = torch.from_numpy(part)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    q.put((rank, t.numpy().tobytes()))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("H", [64, 35])
+def test_row_parallel_projection_sums_to_the_whole_projection_over_gloo(lib, oracle_lib, H):
+    """World 2 on gloo: each rank's heads (oracle), rounded to bf16, times the
+    rank's rows of w_o (zero rows for its padding heads), summed over the
+    ranks, equals the whole projection of the whole attention to fp64
+    rounding.  H = 35 gives rank 1 a padding head whose (nonzero) attention
+    output must not reach the sum."""
+    import torch.multiprocessing as mp
+    world, d_out = 2, 96
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_oproj_worker, args=(r, world, port, H, d_out, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=300) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    c = _case(H)
+    full, _ = oracle_lib.attn(c)
+    ref, absv = oracle_lib.oproj(_bf16_round_f64(full).reshape(c.R, -1), _w_o(H, d_out, 33))
+    for r in range(world):
+        got = np.frombuffer(res[r], np.float64).reshape(ref.shape)
+        assert np.all(np.abs(got - ref) <= 1e-12 * absv + 1e-300)
+
+
+def test_tp_oproj_weights_pad_with_zero_rows(lib):
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    w = torch.arange(35 * 512 * 4, dtype=torch.float32).reshape(35 * 512, 4)
+    w0 = dsa.tp_oproj_weights(w, 35, 2, 0)
+    w1 = dsa.tp_oproj_weights(w, 35, 2, 1)
+    assert w0.data_ptr() == w.data_ptr() and tuple(w0.shape) == (18 * 512, 4)      # a view
+    assert tuple(w1.shape) == (18 * 512, 4)
+    assert torch.equal(w1[:17 * 512], w[18 * 512:]) and not w1[17 * 512:].any()
+
+
+@pytest.mark.gpu
+def test_one_rank_row_parallel_step_equals_the_composed_call(lib):
+    """World 1: attention then projection through tp_sparse_attn_oproj gives
+    the bytes of dsa_sparse_attn_prefill_oproj."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    from gpu_helpers import to_device
+    torch.cuda.set_device(0)
+    c = I.prefill(rows=40, N=2048, first_pos=900)
+    d = to_device(c)
+    w = torch.from_numpy(_w_o(64, 256, 34).view(np.int16)).cuda().view(torch.bfloat16)
+    attn = torch.empty((c.R, 64, 512), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((c.R, 256), dtype=torch.float32, device="cuda")
+    dsa.dsa_sparse_attn_prefill_oproj(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], c.scale, w, attn, out)
+    attn2, out2 = torch.empty_like(attn), torch.empty_like(out)
+    dsa.tp_sparse_attn_oproj(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], c.scale,
+                             dsa.tp_oproj_weights(w, 64, 1, 0), attn2, out2)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("H,world", [(64, 4), (35, 2)])
+def test_row_parallel_shares_on_one_gpu_sum_to_the_projection(lib, oracle_lib, H, world):
+    """The world ranks' shares computed one after the other on one GPU and
+    summed in rank order: within the composed call's bound of the oracle's
+    projection of the oracle's attention, and within the fp32 accumulation
+    bound of the one-GPU projection of the same bf16 attention."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    from gpu_helpers import to_device
+    torch.cuda.set_device(0)
+    c = _case(H)
+    d_out = 128
+    w = _w_o(H, d_out, 35)
+    tw = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
+    total = torch.zeros((c.R, d_out), dtype=torch.float32, device="cuda")
+    for r in range(world):
+        plan = dsa.dsa_head_shard(H, world, r)
+        sc = _shard_case(c, plan)
+        dr = to_device(sc)
+        attn = torch.empty((c.R, plan.heads_per_rank, 512), dtype=torch.bfloat16, device="cuda")
+        part = torch.empty((c.R, d_out), dtype=torch.float32, device="cuda")
+        dsa.tp_sparse_attn_oproj(dr["q"], dr["kv"], dr["idx"], dr["n_sel"], dr["sink"], sc.scale,
+                                 dsa.tp_oproj_weights(tw, H, world, r), attn, part)
+        total += part
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+    got = total.cpu().numpy().astype(np.float64)
+    K = H * 512
+    o, _ = oracle_lib.attn(c)
+    ref, absv = oracle_lib.oproj(o.reshape(c.R, K), w)
+    e_rh = (3e-3 + 2.0 ** -9 * (1 + 3e-3)) * np.abs(o).max(axis=-1)
+    w_abs = np.abs(I.bf16_bits_to_f32(w).astype(np.float64)).reshape(H, 512, d_out).sum(axis=1)
+    lim = e_rh @ w_abs + K * 2.0 ** -24 * absv * (1 + 2 * 3e-3)
+    assert (np.abs(got - ref) <= lim).all(), float(np.max(np.abs(got - ref) / lim))
