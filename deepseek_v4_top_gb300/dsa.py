@@ -403,7 +403,7 @@ def tp_oproj_weights(w_o, H: int, world: int, rank: int):
 
 
 def tp_sparse_attn_oproj(q_local, kv_cache, idx, n_sel, sink_local, scale, w_o_local, attn_local, out,
-                         group=None, rows_per_slot=0, stream=None):
+                         group=None, rows_per_slot=0, stream=None, scatter_out=None):
     """One rank's step of head-sharded attention followed by the output
     projection, row-parallel, all on one stream (torch's current one unless
     `stream` is given): the attention over the rank's heads into attn_local
@@ -414,16 +414,36 @@ def tp_sparse_attn_oproj(q_local, kv_cache, idx, n_sel, sink_local, scale, w_o_l
     tp_sparse_attn followed by the projection, the ranks exchange the
     projected rows (R x d_out fp32) instead of the attention outputs
     (R x H x 512 bf16).  The shares are summed in the collective's order, so
-    the result differs from the one-GPU projection by fp32 rounding."""
+    the result differs from the one-GPU projection by fp32 rounding.
+
+    With `scatter_out` ([R / world, d_out] float32, R a multiple of the world
+    size) the sum is reduce-scattered instead: rank w receives rows
+    [w R / world, (w + 1) R / world) of the projection in scatter_out, and
+    `out` keeps the rank's own unsummed share.  Returns the tensor that holds
+    the summed rows."""
     import torch
     import torch.distributed as dist
     world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
     if attn_local.dtype != torch.bfloat16:
         raise TypeError("attn_local must be bfloat16 (the projection's A operand)")
+    R = attn_local.shape[0]
+    if scatter_out is not None:
+        if (not isinstance(scatter_out, torch.Tensor) or scatter_out.dtype != torch.float32
+                or not scatter_out.is_contiguous() or R % world != 0
+                or tuple(scatter_out.shape) != (R // world, out.shape[-1])):
+            raise ValueError("scatter_out must be a contiguous float32 [rows / world, d_out] tensor, "
+                             "rows a multiple of the world size")
+        _same_device(("out", out), ("scatter_out", scatter_out))
     with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
         dsa_sparse_attn(q_local, kv_cache, idx, n_sel, sink_local, scale, attn_local,
                         rows_per_slot=rows_per_slot)
-        dsa_oproj(attn_local.view(attn_local.shape[0], -1), w_o_local, out)
+        dsa_oproj(attn_local.view(R, -1), w_o_local, out)
+        if scatter_out is not None:
+            if world > 1:
+                dist.reduce_scatter_tensor(scatter_out, out, op=dist.ReduceOp.SUM, group=group)
+            else:
+                scatter_out.copy_(out)
+            return scatter_out
         if world > 1:
             dist.all_reduce(out, op=dist.ReduceOp.SUM, group=group)
         return out

@@ -50,9 +50,9 @@ def test_head_shard_plan_rejects(lib):
         assert e.value.status == st
 
 
-def _case(H):
+def _case(H, rows=3):
     """A small prefill case with H heads (bf16), seeded."""
-    c = I.prefill(seed=31, rows=3, N=700, first_pos=500)
+    c = I.prefill(seed=31, rows=rows, N=700, first_pos=500)
     rng = np.random.default_rng(32)
     c.q = I.f32_to_bf16_bits(rng.standard_normal((c.R, H, 512), dtype=np.float32))
     c.sink = rng.standard_normal(H, dtype=np.float32)
@@ -245,7 +245,7 @@ def _bf16_round_f64(o):
     return I.f32_to_bf16_bits(o.astype(np.float32))
 
 
-def _oproj_worker(rank, world, port, H, d_out, q):
+def _oproj_worker(rank, world, port, H, d_out, q, scatter=False):
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import torch
@@ -254,7 +254,7 @@ def _oproj_worker(rank, world, port, H, d_out, q):
     from deepseek_v4_top_gb300 import dsa
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    c = _case(H)
+    c = _case(H, rows=4 if scatter else 3)
     plan = dsa.dsa_head_shard(H, world, rank)
     local, _ = oracle.attn(_shard_case(c, plan), threads=1)            # [R, hpr, 512], padding heads too
     w = torch.from_numpy(_w_o(H, d_out, 33).view(np.int16))
@@ -262,36 +262,56 @@ def _oproj_worker(rank, world, port, H, d_out, q):
     a = _bf16_round_f64(local).reshape(c.R, -1)
     part, _ = oracle.oproj(a, np.ascontiguousarray(w_local))          # the rank's share, fp64
     t = torch.from_numpy(part)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    if scatter:
+        mine = torch.empty((c.R // world,) + tuple(t.shape[1:]), dtype=t.dtype)
+        dist.reduce_scatter_tensor(mine, t, op=dist.ReduceOp.SUM)
+        t = mine
+    else:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
     q.put((rank, t.numpy().tobytes()))
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("H", [64, 35])
-def test_row_parallel_projection_sums_to_the_whole_projection_over_gloo(lib, oracle_lib, H):
+@pytest.mark.parametrize("H,scatter", [(64, False), (35, False), (35, True)])
+def test_row_parallel_projection_sums_to_the_whole_projection_over_gloo(lib, oracle_lib, H, scatter):
     """World 2 on gloo: each rank's heads (oracle), rounded to bf16, times the
     rank's rows of w_o (zero rows for its padding heads), summed over the
     ranks, equals the whole projection of the whole attention to fp64
     rounding.  H = 35 gives rank 1 a padding head whose (nonzero) attention
-    output must not reach the sum."""
+    output must not reach the sum.  With the reduce-scatter (4 rows) each
+    rank holds its block of rows of that projection."""
     import torch.multiprocessing as mp
     world, d_out = 2, 96
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_oproj_worker, args=(r, world, port, H, d_out, q)) for r in range(world)]
+    procs = [ctx.Process(target=_oproj_worker, args=(r, world, port, H, d_out, q, scatter))
+             for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=300) for _ in range(world))
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    c = _case(H)
+    c = _case(H, rows=4 if scatter else 3)
     full, _ = oracle_lib.attn(c)
     ref, absv = oracle_lib.oproj(_bf16_round_f64(full).reshape(c.R, -1), _w_o(H, d_out, 33))
+    rows = c.R // world if scatter else c.R
     for r in range(world):
-        got = np.frombuffer(res[r], np.float64).reshape(ref.shape)
-        assert np.all(np.abs(got - ref) <= 1e-12 * absv + 1e-300)
+        lo = r * rows if scatter else 0
+        got = np.frombuffer(res[r], np.float64).reshape((rows,) + ref.shape[1:])
+        assert np.all(np.abs(got - ref[lo:lo + rows]) <= 1e-12 * absv[lo:lo + rows] + 1e-300)
+
+
+def test_scatter_out_is_checked_before_any_launch(lib):
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    attn = torch.empty((3, 16, 512), dtype=torch.bfloat16)
+    out = torch.empty((3, 8), dtype=torch.float32)
+    for bad in (torch.empty((2, 8), dtype=torch.float32), torch.empty((3, 8), dtype=torch.float64),
+                torch.empty((3, 16), dtype=torch.float32)[:, ::2]):
+        with pytest.raises(ValueError):
+            dsa.tp_sparse_attn_oproj(None, None, None, None, None, 1.0, None, attn, out, scatter_out=bad)
 
 
 def test_tp_oproj_weights_pad_with_zero_rows(lib):
@@ -308,7 +328,8 @@ def test_tp_oproj_weights_pad_with_zero_rows(lib):
 @pytest.mark.gpu
 def test_one_rank_row_parallel_step_equals_the_composed_call(lib):
     """World 1: attention then projection through tp_sparse_attn_oproj gives
-    the bytes of dsa_sparse_attn_prefill_oproj."""
+    the bytes of dsa_sparse_attn_prefill_oproj, summed in place or into a
+    separate buffer (the reduce-scatter form)."""
     import torch
     from deepseek_v4_top_gb300 import dsa
     from gpu_helpers import to_device
@@ -322,9 +343,14 @@ def test_one_rank_row_parallel_step_equals_the_composed_call(lib):
     attn2, out2 = torch.empty_like(attn), torch.empty_like(out)
     dsa.tp_sparse_attn_oproj(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], c.scale,
                              dsa.tp_oproj_weights(w, 64, 1, 0), attn2, out2)
+    rows = torch.empty_like(out)
+    got = dsa.tp_sparse_attn_oproj(d["q"], d["kv"], d["idx"], d["n_sel"], d["sink"], c.scale,
+                                   dsa.tp_oproj_weights(w, 64, 1, 0), attn2, out2, scatter_out=rows)
     torch.cuda.synchronize()
     assert dsa.dsa_get_device_error() == 0
+    assert got is rows
     assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+    assert torch.equal(out.view(torch.int32), rows.view(torch.int32))
 
 
 @pytest.mark.gpu
