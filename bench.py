@@ -40,6 +40,7 @@ E2E_CHUNKS = 8                              # prefill row chunks in the end-to-e
 OPROJ_D_OUT = 7168                          # output projection width timed (DeepSeek-V3's model width;
                                             # the pages give none for V4.1)
 DEC_B, DEC_N = 8, 32768
+DEC_BIG_B = 608                             # a decode batch that fills the GPU: four rows an SM
 PRE_R, PRE_N = 2048, 4096
 METRIC = "sparse-attn row·heads/s and HBM GB/s at H=64,d=512,k=640 (decode B=8, prefill 2048)"
 WORKLOAD = ("decode B=8 x 1 row (N=32768 per slot) + prefill 2048 rows (positions 2048..4095, "
@@ -343,6 +344,51 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=32):
     assert dsa.dsa_get_device_error() == 0
     assert torch.isfinite(out).all().item()
     return res[0], res[1], res[2]
+
+
+def decode_batch_timing(dsa, dev, flush, B=DEC_BIG_B, reps=16):
+    """Mean milliseconds of one decode call over a batch that fills the GPU
+    (B slots of a 32768-position cache, one row each, k=640), split into
+    128-key chunks (dsa_sparse_attn_decode) and with whole rows
+    (dsa_sparse_attn_decode_whole_rows), the L2 flushed before each call.
+    Inputs are seeded N(0,1) bf16 drawn on the device (20 GB of caches at
+    B = 608) and distinct random positions per slot."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xD5A0 + 23)
+    kv = torch.empty((B, DEC_N, D), dtype=torch.bfloat16, device=dev)
+    for b0 in range(0, B, 64):
+        kv[b0:b0 + 64].normal_(generator=g)
+    q = torch.randn((B, H, D), generator=g, device=dev).to(torch.bfloat16)
+    sink = torch.randn(H, generator=g, device=dev)
+    idx = torch.stack([torch.randperm(DEC_N, generator=g, device=dev)[:K] for _ in range(B)]).to(torch.int32)
+    n_sel = torch.full((B,), K, dtype=torch.int32, device=dev)
+    outs = [torch.empty((B, H, D), dtype=torch.float32, device=dev) for _ in range(2)]
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.current_stream()
+    calls = (lambda: dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, scale, outs[0], stream),
+             lambda: dsa.dsa_sparse_attn_decode_whole_rows(q, kv, idx, n_sel, sink, scale, outs[1], 1, stream))
+    res = []
+    for fn in calls:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        hold_gpu(stream)
+        for i in range(reps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        res.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps)
+    assert dsa.dsa_get_device_error() == 0
+    # the two are the same computation with different rounding orders
+    assert torch.isfinite(outs[1]).all().item()
+    assert (outs[0] - outs[1]).abs().max().item() <= 1e-3 * outs[0].abs().max().item()
+    del kv
+    torch.cuda.empty_cache()
+    return res[0], res[1]
 
 
 def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=32):
@@ -753,6 +799,24 @@ def bench_ours(args, world, rank, local):
             "gathered_frac_hbm": g / (mean * 1e-3) / 1e9 / pk["hbm_gbs"],
             "how": "dsa_sparse_attn_decode, 1 row, 64 heads, N=4096, 640 sorted keys, one call a time, "
                    "L2 flushed before each (split kernel + combine)"}
+        # a decode batch that fills the GPU, split and whole-row (not part of the step)
+        split_ms, whole_ms = decode_batch_timing(dsa, dev, flush)
+        for key, t_ms, how in (
+                ("decode_b%d_split" % DEC_BIG_B, split_ms,
+                 "dsa_sparse_attn_decode (128-key chunks on separate SMs, then the merge kernel)"),
+                ("decode_b%d_whole_rows" % DEC_BIG_B, whole_ms,
+                 "dsa_sparse_attn_decode_whole_rows (each row whole in one CTA, no partials)")):
+            t_ms = reduce_max(t_ms, world)
+            g = DEC_BIG_B * K * D * 2
+            cb = compulsory_bytes(DEC_BIG_B, g)
+            workloads[key] = {
+                "ms": t_ms, "row_heads_per_s": DEC_BIG_B * H / (t_ms * 1e-3),
+                "gathered_kv_gbs": g / (t_ms * 1e-3) / 1e9,
+                "gathered_frac_hbm": g / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "compulsory_bytes": cb, "compulsory_gbs": cb / (t_ms * 1e-3) / 1e9,
+                "compulsory_frac_hbm": cb / (t_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "how": how + ", %d slots x 1 row, N=32768 per slot, k=640, one call a time, L2 flushed "
+                             "before each; inputs drawn on the device" % DEC_BIG_B}
         # the indexer's top-k selection, timed on its own (not part of the step)
         for mode, key in (("prefill", "topk_prefill_2048"), ("decode", "topk_decode_b8")):
             t_ms, rows, nbytes = topk_timing(dsa, dev, flush, mode)

@@ -136,10 +136,13 @@ dsa_status check_args(const void* q, const void* kv, const int32_t* idx, const i
 }
 
 // decode: 0 for prefill (one cache shared by every row), T >= 1 for decode
-// with T query rows a slot (row r reads slot r / T).
+// with T query rows a slot (row r reads slot r / T).  split: a decode row's
+// keys run as 128-key chunks on several SMs and are merged; otherwise each
+// row runs whole in one CTA, as a prefill row does.
 dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t* n_sel,
                const float* sink, float scale, void* out, int R, int H, int N, int k_max,
-               dsa_dtype dtype, void* stream, int decode, dsa_dtype out_dtype = DSA_F32) {
+               dsa_dtype dtype, void* stream, int decode, dsa_dtype out_dtype = DSA_F32,
+               bool split = true) {
     if (out_dtype != DSA_F32 && out_dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
     dsa_status st = check_args(q, kv, idx, n_sel, sink, out, R, H, N, k_max, dtype, decode);
     if (st != DSA_OK || R == 0) return st;
@@ -185,7 +188,7 @@ dsa_status run(const void* q, const void* kv, const int32_t* idx, const int32_t*
     p.N = N;
     p.k_max = k_max;
     p.decode = decode;
-    const int chunks = decode ? (k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys : 1;
+    const int chunks = decode && split ? (k_max + kDecodeChunkKeys - 1) / kDecodeChunkKeys : 1;
     p.chunk_keys = chunks > 1 ? kDecodeChunkKeys : k_max;
     p.chunks = chunks;
     p.units = R * chunks;
@@ -247,6 +250,15 @@ dsa_status dsa_sparse_attn(const void* q, const void* kv_cache, const int32_t* i
     if (R < 0 || rows_per_slot < 0 || (rows_per_slot > 0 && R % rows_per_slot != 0)) return DSA_ERR_INVALID_ARG;
     return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, rows_per_slot,
                     out_dtype);
+}
+
+dsa_status dsa_sparse_attn_decode_whole_rows(const void* q, const void* kv_cache, const int32_t* idx,
+                                             const int32_t* n_sel, const float* sink, float scale, void* out,
+                                             int R, int rows_per_slot, int H, int N, int k_max, dsa_dtype dtype,
+                                             dsa_dtype out_dtype, void* stream) {
+    if (R < 0 || rows_per_slot < 1 || R % rows_per_slot != 0) return DSA_ERR_INVALID_ARG;
+    return dsa::run(q, kv_cache, idx, n_sel, sink, scale, out, R, H, N, k_max, dtype, stream, rows_per_slot,
+                    out_dtype, false);
 }
 
 dsa_status dsa_oproj(const void* attn, const void* w_o, float* out, int R, int K, int d_out, void* stream) {

@@ -32,7 +32,7 @@ DSA_DEVERR_NVALID_RANGE = 0x10
 
 # Every function declared in include/dsa.h.
 EXPORTS = ("dsa_sparse_attn_decode", "dsa_sparse_attn_decode_rows", "dsa_sparse_attn_prefill",
-           "dsa_sparse_attn", "dsa_oproj", "dsa_sparse_attn_prefill_oproj",
+           "dsa_sparse_attn", "dsa_sparse_attn_decode_whole_rows", "dsa_oproj", "dsa_sparse_attn_prefill_oproj",
            "dsa_sparse_attn_decode_noalloc",
            "dsa_topk_select", "dsa_head_shard", "dsa_shard_heads", "dsa_unshard_heads",
            "dsa_selftest_wait_limit", "dsa_get_device_error", "dsa_status_string", "dsa_shutdown")
@@ -73,6 +73,8 @@ def load():
             lib.dsa_sparse_attn_decode_rows.restype = I
             lib.dsa_sparse_attn.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, P]
             lib.dsa_sparse_attn.restype = I
+            lib.dsa_sparse_attn_decode_whole_rows.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, P]
+            lib.dsa_sparse_attn_decode_whole_rows.restype = I
             lib.dsa_oproj.argtypes = [P, P, P, I, I, I, P]
             lib.dsa_oproj.restype = I
             lib.dsa_sparse_attn_prefill_oproj.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I, I, P]
@@ -235,6 +237,29 @@ def dsa_sparse_attn(q, kv_cache, idx, n_sel, sink, scale, out, rows_per_slot=0, 
                                 k_max, _dtype_code(q), _dtype_code(out), _stream_handle(stream))
     if st != DSA_OK:
         raise DsaError(st, "dsa_sparse_attn")
+    return out
+
+
+def dsa_sparse_attn_decode_whole_rows(q, kv_cache, idx, n_sel, sink, scale, out, rows_per_slot=1, stream=None):
+    """Decode without the key split (each row whole in one CTA, no partials):
+    q [B*T,H,512], kv_cache [B,N,512], idx [B*T,k_max], n_sel [B*T], out
+    [B*T,H,512] float32 or bfloat16; row r reads slot r // T (T =
+    rows_per_slot).  For batches of about as many rows as SMs or more."""
+    import torch
+    T = int(rows_per_slot)
+    if T < 1:
+        raise ValueError("rows_per_slot must be >= 1")
+    if not isinstance(out, torch.Tensor) or out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be a float32 or bfloat16 tensor")
+    if kv_cache.dim() != 3 or q.dim() != 3 or q.shape[0] != kv_cache.shape[0] * T:
+        raise ValueError("q must be [slots * rows_per_slot, heads, 512] for kv_cache [slots, N, 512]")
+    R, H, N, k_max = _check(q, kv_cache, idx, n_sel, sink, out, decode=True, rows_per_slot=T, out_dtype=out.dtype)
+    st = load().dsa_sparse_attn_decode_whole_rows(q.data_ptr(), kv_cache.data_ptr(), idx.data_ptr(),
+                                                  n_sel.data_ptr(), sink.data_ptr(), ctypes.c_float(float(scale)),
+                                                  out.data_ptr(), R, T, H, N, k_max, _dtype_code(q),
+                                                  _dtype_code(out), _stream_handle(stream))
+    if st != DSA_OK:
+        raise DsaError(st, "dsa_sparse_attn_decode_whole_rows")
     return out
 
 

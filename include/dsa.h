@@ -167,6 +167,35 @@ DSA_API dsa_status dsa_sparse_attn(const void* q, const void* kv_cache,
                                    dsa_dtype dtype, dsa_dtype out_dtype, void* stream);
 
 /*
+ * Decode without the key split, for batches large enough to fill the GPU:
+ * row r (rows_per_slot >= 1 rows a slot, R a multiple of it) reads slot
+ * r / rows_per_slot of kv [R / rows_per_slot][N][512], and each row's keys
+ * run from first to last in one CTA, as a prefill row's do, with rows handed
+ * out by the stream's row queue.  dsa_sparse_attn_decode splits every row
+ * into 128-key chunks on separate SMs and merges their partials (128 KB of
+ * fp32 each) in a second kernel: at 8 rows that spreads the work over 40 SMs,
+ * but once there are about as many rows as SMs the partials only add traffic
+ * (and stop fitting in the L2).  This call writes no partials and launches
+ * one kernel.
+ * Results: the same computation as dsa_sparse_attn_decode (running maximum,
+ * tile sum and value sum over the selected keys, the sink folded into the
+ * denominator), with one running softmax over the whole row instead of
+ * chunks merged, so the bits differ from that call's within the same
+ * tolerance.  They do not depend on the batch, and they equal, bit for bit,
+ * dsa_sparse_attn_prefill's over the slots' caches viewed as one cache
+ * [R / rows_per_slot * N][512] with each row's indices offset by its slot
+ * times N.  fp32 inputs run the fp32 kernel, which never splits (the same
+ * bits as dsa_sparse_attn_decode_rows).  Arguments, layouts, ownership and
+ * errors as dsa_sparse_attn (out_dtype DSA_F32 or DSA_BF16); rows_per_slot
+ * < 1 or R not a multiple of it is DSA_ERR_INVALID_ARG.
+ */
+DSA_API dsa_status dsa_sparse_attn_decode_whole_rows(const void* q, const void* kv_cache,
+                                                     const int32_t* idx, const int32_t* n_sel,
+                                                     const float* sink, float scale, void* out,
+                                                     int R, int rows_per_slot, int H, int N, int k_max,
+                                                     dsa_dtype dtype, dsa_dtype out_dtype, void* stream);
+
+/*
  * Output projection of attention rows (the step after the attention: the
  * heads' outputs of a row, concatenated, times the projection matrix):
  *   attn [R][K] bfloat16 (for this library's output, K = H*512 and the

@@ -122,6 +122,20 @@ def test_general_call_and_projection_host_validation(lib):
     assert attn(out=FAKE + 2) == dsa.DSA_ERR_INVALID_ARG       # misaligned out
     assert attn(R=0, q=0, out=0) == dsa.DSA_OK
 
+    def whole(**kw):
+        a = dict(q=FAKE, kv=FAKE, idx=FAKE, n_sel=FAKE, sink=FAKE, out=FAKE, R=4, T=1, out_dtype=dsa.DSA_F32)
+        a.update(kw)
+        return lib.dsa_sparse_attn_decode_whole_rows(a["q"], a["kv"], a["idx"], a["n_sel"], a["sink"], 0.1,
+                                                     a["out"], a["R"], a["T"], 64, 100, 8, dsa.DSA_BF16,
+                                                     a["out_dtype"], None)
+    assert whole(T=0) == dsa.DSA_ERR_INVALID_ARG               # decode needs rows_per_slot >= 1
+    assert whole(T=3) == dsa.DSA_ERR_INVALID_ARG               # rows not a multiple of rows_per_slot
+    assert whole(R=-1) == dsa.DSA_ERR_INVALID_ARG
+    for ptr in ("q", "kv", "idx", "n_sel", "sink", "out"):
+        assert whole(**{ptr: 0}) == dsa.DSA_ERR_INVALID_ARG
+    assert whole(out_dtype=7) == dsa.DSA_ERR_UNSUPPORTED
+    assert whole(R=0, q=0, out=0) == dsa.DSA_OK
+
     def proj(**kw):
         a = dict(attn=FAKE, w=FAKE, out=FAKE, R=4, K=512, d_out=64)
         a.update(kw)
