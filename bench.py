@@ -346,9 +346,9 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=32):
     return res[0], res[1], res[2]
 
 
-def decode_batch_timing(dsa, dev, flush, B=DEC_BIG_B, reps=16):
+def decode_batch_timing(dsa, dev, flush, B=DEC_BIG_B, reps=16, N=DEC_N):
     """Mean milliseconds of one decode call over a batch that fills the GPU
-    (B slots of a 32768-position cache, one row each, k=640), split into
+    (B slots of an N-position cache, one row each, k=640), split into
     128-key chunks (dsa_sparse_attn_decode) and with whole rows
     (dsa_sparse_attn_decode_whole_rows), the L2 flushed before each call.
     Inputs are seeded N(0,1) bf16 drawn on the device (20 GB of caches at
@@ -356,12 +356,12 @@ def decode_batch_timing(dsa, dev, flush, B=DEC_BIG_B, reps=16):
     import torch
     g = torch.Generator(device=dev)
     g.manual_seed(0xD5A0 + 23)
-    kv = torch.empty((B, DEC_N, D), dtype=torch.bfloat16, device=dev)
+    kv = torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)
     for b0 in range(0, B, 64):
         kv[b0:b0 + 64].normal_(generator=g)
     q = torch.randn((B, H, D), generator=g, device=dev).to(torch.bfloat16)
     sink = torch.randn(H, generator=g, device=dev)
-    idx = torch.stack([torch.randperm(DEC_N, generator=g, device=dev)[:K] for _ in range(B)]).to(torch.int32)
+    idx = torch.stack([torch.randperm(N, generator=g, device=dev)[:K] for _ in range(B)]).to(torch.int32)
     n_sel = torch.full((B,), K, dtype=torch.int32, device=dev)
     outs = [torch.empty((B, H, D), dtype=torch.float32, device=dev) for _ in range(2)]
     scale = 1.0 / math.sqrt(D)
@@ -470,6 +470,31 @@ def bench_decode_rows(args, world, rank, local):
         print(json.dumps({"metric": "decode with %d rows a slot, ms per call" % T, "ms": t_ms, "rows": rows,
                           "selected_kv_bytes": int(c.n_sel.astype(np.int64).sum()) * D * 2,
                           "distinct_kv_bytes": distinct * D * 2}), flush=True)
+
+
+def bench_decode_batch(args, world, rank, local):
+    """A decode batch that fills the GPU alone (for profiling): --slots slots
+    of --slot-positions positions, split and whole-row calls, --steps timed
+    calls of each; one JSON line with both times and their HBM fractions."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    import __graft_entry__
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    __graft_entry__.build()
+    dsa.load()
+    pk, _ = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    B, N = args.slots, args.slot_positions
+    split_ms, whole_ms = decode_batch_timing(dsa, dev, flush, B=B, reps=max(1, args.steps), N=N)
+    g = B * K * D * 2
+    if rank == 0:
+        print(json.dumps({"metric": "decode batch, ms per call (L2 flushed before each)", "slots": B,
+                          "positions_per_slot": N, "split_ms": split_ms, "whole_rows_ms": whole_ms,
+                          "gathered_bytes": g, "compulsory_bytes": compulsory_bytes(B, g),
+                          "whole_rows_gathered_frac_hbm": g / (whole_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "split_gathered_frac_hbm": g / (split_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}), flush=True)
 
 
 def bench_topk(args, world, rank, local):
@@ -1093,10 +1118,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk", "decode_rows", "oproj"),
+    ap.add_argument("--workload", choices=("both", "prefill", "decode", "topk", "decode_rows", "oproj",
+                                           "decode_batch"),
                     default="both",
                     help="both (the benchmark step), one half of it for profiling, the top-k "
-                         "selection alone, or decode with --rows-per-slot rows a slot alone")
+                         "selection alone, decode with --rows-per-slot rows a slot alone, or a decode "
+                         "batch of --slots slots alone (split and whole-row calls)")
+    ap.add_argument("--slots", type=int, default=DEC_BIG_B, help="slots of the decode_batch workload")
+    ap.add_argument("--slot-positions", type=int, default=DEC_N,
+                    help="positions a slot of the decode_batch workload (a smaller cache for profiling)")
     ap.add_argument("--rows-per-slot", type=int, default=2,
                     help="rows a slot of the decode_rows workload")
     ap.add_argument("--oproj-k", type=int, default=H * D,
@@ -1114,6 +1144,8 @@ def main(argv=None):
         bench_topk(args, world, rank, local)
     elif args.workload == "decode_rows":
         bench_decode_rows(args, world, rank, local)
+    elif args.workload == "decode_batch":
+        bench_decode_batch(args, world, rank, local)
     elif args.workload == "oproj":
         bench_oproj(args, world, rank, local)
     elif args.tp:
