@@ -175,3 +175,44 @@ def test_split_decode_with_more_units_than_sms_keeps_its_bits():
     ref, _ = oracle.attn(I.Case("some", "decode", c.dtype, 8, c.H, c.N, c.k_max, c.q[:8], c.kv[:8],
                                 c.idx[:8], c.n_sel[:8], c.sink, c.scale))
     compare(c, big[:8], ref)
+
+
+def test_full_size_batch_sampled_against_the_oracle():
+    """The bench's large decode batch in its own launch configuration (608
+    slots of 32768 positions, k = 640, inputs drawn on the device): sampled
+    rows of the whole-row call and of the split call against the oracle.
+    Each sampled row's selected KV rows are copied out in index order, so
+    the oracle reads exactly the rows the kernels gathered, in that order."""
+    import torch
+    from deepseek_v4_top_gb300 import dsa
+    B, N, K, H, D = 608, 32768, 640, 64, 512
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0xD5A0 + 29)
+    kv = torch.empty((B, N, D), dtype=torch.bfloat16, device=dev)
+    for b0 in range(0, B, 64):
+        kv[b0:b0 + 64].normal_(generator=g)
+    q = torch.randn((B, H, D), generator=g, device=dev).to(torch.bfloat16)
+    sink = torch.randn(H, generator=g, device=dev)
+    idx = torch.stack([torch.randperm(N, generator=g, device=dev)[:K] for _ in range(B)]).to(torch.int32)
+    n_sel = torch.full((B,), K, dtype=torch.int32, device=dev)
+    n_sel[5] = 0
+    n_sel[300] = 129
+    whole = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    split = torch.empty_like(whole)
+    scale = 1.0 / np.sqrt(D)
+    dsa.dsa_sparse_attn_decode_whole_rows(q, kv, idx, n_sel, sink, scale, whole)
+    dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, scale, split)
+    assert dsa.dsa_get_device_error() == 0
+    rows = [0, 5, 151, 152, 300, 455, 607]
+    sel = idx[rows].long()
+    gathered = torch.stack([kv[r][sel[i]] for i, r in enumerate(rows)])      # [rows, K, D] in index order
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    c = I.Case("b608_sample", "decode", I.BF16, len(rows), H, K, K, bits(q[rows]), bits(gathered),
+               np.tile(np.arange(K, dtype=np.int32), (len(rows), 1)), n_sel[rows].cpu().numpy(),
+               sink.cpu().numpy(), scale)
+    ref, _ = oracle.attn(c)
+    compare(c, whole[rows].cpu().numpy(), ref)
+    compare(c, split[rows].cpu().numpy(), ref)
+    del kv
+    torch.cuda.empty_cache()
