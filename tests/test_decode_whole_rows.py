@@ -66,6 +66,28 @@ def test_whole_rows_match_the_oracle(B, T):
     compare(c, got, ref)
 
 
+@pytest.mark.parametrize("H,k,T", [(16, 77, 1), (32, 2048, 2), (64, 1, 1), (16, 129, 3)])
+def test_whole_rows_other_head_counts_and_selection_sizes(H, k, T):
+    """16 and 32 heads, one key, a partial tile, and 2048 keys (16 tiles a
+    row): parity with the oracle and bit-identity with the prefill call over
+    the flattened caches."""
+    c = I.multi_row_decode(B=3, T=T, N=max(2 * k, 300), k=k, H=H, seed=790 + k + H)
+    c.n_sel[-1] = max(k // 2, 1)
+    got, code = _whole(c)
+    assert code == 0
+    ref, _ = oracle.attn(c)
+    compare(c, got, ref)
+    slot = np.arange(c.R) // T
+    idx = c.idx.copy()
+    for r in range(c.R):
+        idx[r, :c.n_sel[r]] += slot[r] * c.N
+    flat = I.Case("flat", "prefill", c.dtype, c.R, c.H, c.kv.shape[0] * c.N, c.k_max, c.q,
+                  c.kv.reshape(-1, 512), idx, c.n_sel, c.sink, c.scale)
+    want, code = run(flat)
+    assert code == 0
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 def test_whole_rows_fp32_inputs_give_the_decode_rows_bits():
     c = I.multi_row_decode(B=2, T=2, N=600, k=200, dtype=I.F32, H=16, seed=720)
     got, code = _whole(c)
