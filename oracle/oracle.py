@@ -41,11 +41,16 @@ def build(force: bool = False) -> str:
 
 
 def load():
+    """The oracle library.  DSA_ORACLE_LIB, when set, names another build of
+    dsa_oracle.c to load instead (the planted-mistake copies of
+    tests/test_oracle_mutants.py, which must fail the pins)."""
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(LIB_PATH)
+            path = os.environ.get("DSA_ORACLE_LIB") or LIB_PATH
+            if path == LIB_PATH:
+                build()
+            lib = ctypes.CDLL(path)
             P = ctypes.c_void_p
             I = ctypes.c_int
             F = ctypes.c_float
