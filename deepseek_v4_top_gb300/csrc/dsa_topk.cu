@@ -81,6 +81,12 @@ struct TopkSmem {
 template <int kBinsPerThread>
 __device__ __forceinline__ int bin_slot(uint32_t d) { return static_cast<int>(d + d / kBinsPerThread); }
 
+// The sum of the totals of the warps before this one (warp_sum holds one a
+// warp): lane w < warp reads warp w's, and the warp adds them up at once.
+__device__ __forceinline__ uint32_t earlier_warps(const uint32_t* warp_sum, int warp, int lane) {
+    return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? warp_sum[lane] : 0u);
+}
+
 // The digit passes: bits [21, 32), [10, 21), [0, 10).
 __device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
 __device__ __forceinline__ int digit_bins(int pass) { return pass == 2 ? 1024 : 2048; }
@@ -243,9 +249,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
             __syncthreads();
 #pragma unroll
             for (int b = 0; b < kB; ++b) sm.hist[bin_slot<kB>(tid * kB + b)] = 0u;
-            uint32_t before = 0u;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) before += w < warp ? sm.warp_sum[w] : 0u;
+            const uint32_t before = earlier_warps(sm.warp_sum, warp, lane);
             const uint32_t excl = before + incl - sum;
             if (excl < want && want <= excl + sum) {
                 uint32_t above = excl;
@@ -292,9 +296,7 @@ __global__ void __launch_bounds__(kThreads, kMode == kCandToIdx ? 1 : (kThreads 
         }
         if (lane == 31) sm.warp_sum[warp] = incl;
         __syncthreads();
-        uint32_t before = incl - packed;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) before += w < warp ? sm.warp_sum[w] : 0u;
+        const uint32_t before = incl - packed + earlier_warps(sm.warp_sum, warp, lane);
         const uint32_t eq_before = before & 0xFFFFu;
         int at = static_cast<int>((before >> 16) + (eq_before < need ? eq_before : need));
         // writes pick i at output entry `at`
