@@ -273,6 +273,23 @@ def hold_gpu(stream, ms=4.0):
         torch.cuda._sleep(int(ms * 2.0e6))      # cycles at about 2 GHz
 
 
+def cold_call_ms(fn, flush, stream, reps):
+    """Milliseconds of `reps` calls of fn() on `stream` (torch's current
+    one), each after an L2-flushing write and bracketed by its own events.
+    The stream is held first, so that the host has queued the calls before
+    the GPU reaches them."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    hold_gpu(stream)
+    for i, (e0, e1) in enumerate(ev):
+        flush.fill_(float(i))
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
 def topk_timing(dsa, dev, flush, mode, k=K, reps=32):
     """Mean milliseconds of one top-k selection call over the indexer-score
     rows of `mode` (prefill: 2048 causal rows of a 4096 cache; decode: 8
@@ -289,15 +306,7 @@ def topk_timing(dsa, dev, flush, mode, k=K, reps=32):
     for _ in range(3):
         dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    hold_gpu(stream)
-    for i in range(reps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = cold_call_ms(lambda: dsa.dsa_topk_select(s, nv, k, idx, n_sel, stream), flush, stream, reps)
     assert dsa.dsa_get_device_error() == 0
     return sum(ms) / reps, R, int(n_valid.astype(np.int64).sum()) * 4
 
@@ -334,15 +343,7 @@ def oproj_timing(dsa, dev, flush, d_pre, pre, d_out=OPROJ_D_OUT, reps=32):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        hold_gpu(stream)
-        for i in range(reps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            fn()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        res.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps)
+        res.append(sum(cold_call_ms(fn, flush, stream, reps)) / reps)
     assert dsa.dsa_get_device_error() == 0
     assert torch.isfinite(out).all().item()
     return res[0], res[1], res[2]
@@ -375,15 +376,7 @@ def decode_batch_timing(dsa, dev, flush, B=DEC_BIG_B, reps=16, N=DEC_N):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        hold_gpu(stream)
-        for i in range(reps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            fn()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        res.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps)
+        res.append(sum(cold_call_ms(fn, flush, stream, reps)) / reps)
     assert dsa.dsa_get_device_error() == 0
     # the two are the same computation with different rounding orders
     assert torch.isfinite(outs[1]).all().item()
@@ -406,15 +399,8 @@ def decode_rows_timing(dsa, dev, flush, B=DEC_B, T=2, reps=32):
     for _ in range(3):
         dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    hold_gpu(stream)
-    for i in range(reps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = cold_call_ms(lambda: dsa.dsa_sparse_attn_decode_rows(q, kv, idx, n_sel, sink, c.scale, out, T, stream),
+                      flush, stream, reps)
     assert dsa.dsa_get_device_error() == 0
     return sum(ms) / reps, c.R
 
@@ -433,15 +419,8 @@ def single_decode_timing(dsa, dev, flush, reps=32):
     for _ in range(3):
         dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, c.scale, out, stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    hold_gpu(stream)
-    for i in range(reps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, c.scale, out, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = cold_call_ms(lambda: dsa.dsa_sparse_attn_decode(q, kv, idx, n_sel, sink, c.scale, out, stream),
+                      flush, stream, reps)
     assert dsa.dsa_get_device_error() == 0
     return statistics.median(ms), sum(ms) / reps
 
@@ -550,16 +529,8 @@ def bench_oproj(args, world, rank, local):
             flush.fill_(0.5)
             fn()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(max(1, args.steps))]
-        hold_gpu(stream)
-        for i, (e0, e1) in enumerate(ev):
-            flush.fill_(float(i))
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / len(ev)
+        ms_list = cold_call_ms(fn, flush, stream, max(1, args.steps))
+        ms = sum(ms_list) / len(ms_list)
         res[name] = {"ms": ms, "tflops": 2.0 * PRE_R * Kp * N / (ms * 1e-3) / 1e12}
     assert dsa.dsa_get_device_error() == 0
     if rank == 0:
