@@ -238,3 +238,24 @@ def test_full_size_batch_sampled_against_the_oracle():
     compare(c, split[rows].cpu().numpy(), ref)
     del kv
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", I.EDGE_SPECIALS)
+def test_whole_rows_nonfinite_specials_match_the_oracle_and_repeat(name):
+    """The edge sweep's nine special cases (NaN and infinities in q or in a
+    selected row, NaN in every unselected row, -inf and zero sinks) as
+    decode batches through the whole-row call: the oracle's classes and
+    tolerance, and five runs with the same bits.  A prefill case becomes a
+    decode batch whose slots each hold a copy of its cache."""
+    c = I.edge_special(name, (I.SEED_BASE + 4) * 131 + 700 + I.EDGE_SPECIALS.index(name))
+    if c.mode == "prefill":
+        kv = np.ascontiguousarray(np.broadcast_to(c.kv, (c.R,) + c.kv.shape))
+        c = I.Case(c.name, "decode", c.dtype, c.R, c.H, c.N, c.k_max, c.q, kv, c.idx, c.n_sel, c.sink, c.scale)
+    d = to_device(c)
+    got, code = _whole(c, d)
+    assert code == 0
+    ref, _ = oracle.attn(c)
+    compare(c, got, ref)
+    for _ in range(4):
+        again, code = _whole(c, d)
+        assert code == 0 and np.array_equal(again.view(np.uint32), got.view(np.uint32))
